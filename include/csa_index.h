@@ -1,0 +1,189 @@
+/*
+ * csa_index.h — C ABI of the CSA indexer hot path for GB300 (sm_103a).
+ *
+ * What the library computes (FlashMemory-DeepSeek-V4, "Retriever architecture"
+ * and "compressed_k format"): for every query row b and every visible record n
+ * of a paged compressed-K cache,
+ *
+ *     k_n[d]   = e4m3(rec_n[d]) * scale_n          d < 128, scale_n = fp32 at bytes 128..131
+ *     logit_bn = sum_h relu(k_n . q_b[h]) * fused_w_b[h]
+ *     score_bn = sigmoid(logit_bn)                 in [0, 1]
+ *
+ * and keeps the top-k records of each query ("Two-level recall algorithm",
+ * Level 2: the top-512 is taken over the whole history or, with non-resident
+ * logits masked to -inf, over a resident page subset).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer handed to a compute entry point is DEVICE memory owned by the
+ *   caller, except the args struct itself, which is read on the host during the
+ *   call only. The library never allocates, frees, synchronises or reads device
+ *   data on the host; all work is enqueued on `stream` (a cudaStream_t passed as
+ *   void*, NULL = legacy default stream). The only state it keeps is a one-time
+ *   per-device kernel attribute set-up (dynamic shared memory size) and the
+ *   device's SM count; both are taken on the first call on a device.
+ * - Calls are re-entrant and capturable in a CUDA graph as long as their
+ *   workspaces do not overlap while in flight.
+ * - Host-detectable errors return a csa_status and launch nothing.
+ *   Data-dependent errors found on the device never trap: they OR a CSA_DEV_*
+ *   bit into *dev_status (when given) and the offending page or query is left
+ *   out of the result.
+ *
+ * Cache geometry ("compressed_k format"): a record is 132 bytes, 128 e4m3 bytes
+ * (OCP FP8 E4M3, the `float8_e4m3fn` variant: bias 7, max 448, S.1111.111 = NaN)
+ * followed by a little-endian IEEE fp32 scale. 64 records form a page; pages
+ * sit at `page_stride_bytes` apart (>= 64*132, a multiple of 16, so allocator
+ * padding is allowed, as the geometry guard of the BatchGen #153 commit log asks
+ * for).
+ *
+ * Lengths (`q_len`) count compressed records, not tokens (BatchGen #153 commit
+ * log: passing raw token counts to the c4 indexer read 4x out of bounds).
+ */
+#ifndef CSA_INDEX_H
+#define CSA_INDEX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA_ABI_VERSION 1
+
+#define CSA_HEAD_DIM 128        /* D: e4m3 bytes per record                         */
+#define CSA_NUM_HEADS 64        /* H of the Level-2 indexer                         */
+#define CSA_RECORD_BYTES 132    /* D + 4-byte fp32 scale                            */
+#define CSA_PAGE_RECORDS 64     /* records per page                                 */
+#define CSA_PAGE_BYTES 8448     /* 64 * 132                                         */
+#define CSA_MAX_K 1024          /* largest top-k supported                          */
+#define CSA_MAX_CTAS 1024       /* upper bound on the persistent grid, sizes slots  */
+
+typedef enum csa_status {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, k out of [1, CSA_MAX_K] ...   */
+  CSA_ERR_UNSUPPORTED = 2,   /* head_dim != 128 or num_heads != 64, too many SMs            */
+  CSA_ERR_ALIGNMENT = 3,     /* a pointer or stride breaks the alignment stated below       */
+  CSA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than csa_index_workspace_bytes()  */
+  CSA_ERR_CUDA = 5           /* a CUDA runtime call failed (launch, attribute, device query) */
+} csa_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+enum {
+  CSA_DEV_PAGE_OOB = 1,      /* page_table entry outside [0, num_pages): page skipped      */
+  CSA_DEV_RESIDENT_OOB = 2,  /* resident page id outside [0, ceil(len/64)): page skipped  */
+  CSA_DEV_RANGE = 4,         /* q holds a non-finite value                                 */
+  CSA_DEV_TIMEOUT = 8,       /* an on-chip pipeline wait ran past its limit; output invalid */
+  CSA_DEV_BAD_REQUEST = 16,  /* q_req entry outside [0, num_req): query treated as empty   */
+  CSA_DEV_LEN_OOB = 32       /* q_len < 0, q_len > 64*pt_stride, or n_resident outside
+                                [0, res_stride]: clamped                                  */
+};
+
+/*
+ * Inputs of one indexer call.
+ *
+ * q          [num_q, num_heads, head_dim] bf16, contiguous, 16-byte aligned. The indexer
+ *            query after its projection/RoPE/Hadamard chain (FlashMemory-DeepSeek-V4,
+ *            "Retriever architecture"). Any finite bf16 value is accepted.
+ * fused_w    [num_q, num_heads] fp32, contiguous, 4-byte aligned: weights_proj output
+ *            already multiplied by head_dim^-0.5 * num_heads^-0.5.
+ * kv         [num_pages] pages of 64 records, `page_stride_bytes` apart, 16-byte aligned.
+ * page_table [num_req, pt_stride] int32: logical page -> physical page of each request.
+ * q_req      [num_q] int32 request of each query row, or NULL for the identity map
+ *            (decode: row b reads request b; then num_req must be >= num_q).
+ * q_len      [num_q] int32 visible compressed records of each query row. Several rows may
+ *            share one request with different bounds (chunked prefill), so the bound is
+ *            per row ("DeepSeek-V4.1 native paged runtime", "Current execution scope":
+ *            one scorer, each query row with its own bound and tile list).
+ * resident   [num_req, res_stride] int32 logical page ids to score, or NULL to score
+ *            the whole history [0, q_len). Pages of one request must be distinct.
+ * n_resident [num_req] int32 entries used in each resident row (required iff resident).
+ * dev_status optional int32 in device memory; kernels OR CSA_DEV_* bits into it.
+ *
+ * Visible records of row b (req = q_req[b], L = min(q_len[b], 64*pt_stride)):
+ *   full mode      positions n in [0, L)
+ *   resident mode  positions p*64 + r for each listed page p, r < 64, p*64 + r < L
+ * The position n is the record's logical index in the request's history; it is what
+ * top-k returns.
+ */
+typedef struct csa_index_args {
+  const void* q;
+  const float* fused_w;
+  int32_t num_q;
+  int32_t num_heads;
+  int32_t head_dim;
+  int32_t reserved0;         /* must be 0 */
+  const uint8_t* kv;
+  int64_t num_pages;
+  int64_t page_stride_bytes;
+  const int32_t* page_table;
+  int32_t num_req;
+  int32_t pt_stride;
+  const int32_t* q_req;
+  const int32_t* q_len;
+  const int32_t* resident;
+  const int32_t* n_resident;
+  int32_t res_stride;
+  int32_t reserved1;         /* must be 0 */
+  int32_t* dev_status;
+} csa_index_args;
+
+/* CSA_ABI_VERSION of the loaded library. */
+int32_t csa_index_abi_version(void);
+
+/* Static description of a status code; never NULL. */
+const char* csa_status_str(csa_status s);
+
+/*
+ * Bytes of device workspace that csa_index_topk and csa_index_score_topk_fused need for
+ * these arguments and this k. Pure host arithmetic on num_q and k (no device access).
+ * Returns 0 when num_q < 0 or k is outside [1, CSA_MAX_K].
+ */
+size_t csa_index_workspace_bytes(const csa_index_args* args, int32_t k);
+
+/*
+ * Scores of every visible record ("Retriever architecture": score = sigmoid of the
+ * relu'd, head-weighted sum).
+ *
+ * scores  [num_q, score_stride] fp32 device memory, 4-byte aligned. Row b, column c:
+ *           full mode      c = logical position n, for n < L
+ *           resident mode  c = j*64 + r for the j-th listed page, row r
+ *         Columns of invisible records are not written.
+ * score_stride >= the largest column written + 1 (full: 64*pt_stride; resident:
+ *         64*res_stride is always enough).
+ * Errors: CSA_ERR_INVALID_ARG (null pointers, negative sizes, score_stride too small for
+ * 64*pt_stride / 64*res_stride), CSA_ERR_UNSUPPORTED, CSA_ERR_ALIGNMENT, CSA_ERR_CUDA.
+ */
+csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t score_stride,
+                           void* stream);
+
+/*
+ * Top-k over a caller-provided score matrix laid out as csa_index_score writes it
+ * (the "Top-k Selector" of "Two-level recall algorithm", Level 2). Only the bounds
+ * fields of `args` are read: num_q, num_req, q_req, q_len, resident, n_resident,
+ * res_stride, pt_stride, dev_status (q, fused_w, kv and page_table may be NULL).
+ *
+ * idx  [num_q, k] int32: logical positions sorted by (score desc, position asc);
+ *      rows with fewer than k visible records are padded with -1.
+ * vals [num_q, k] fp32: the matching scores; padding is 0.0f.
+ * ws   device workspace of at least csa_index_workspace_bytes(args, k) bytes, 16-byte
+ *      aligned. Contents on entry are ignored; it must not be shared by calls in flight.
+ */
+csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_index_args* args,
+                          int32_t k, int32_t* idx, float* vals, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/*
+ * Fused score + top-k: the scores never leave the chip ("Two-level recall algorithm",
+ * Level 2, masked or full). Records are ranked by (logit desc, position asc), which is
+ * the score order because sigmoid is monotone; vals hold sigmoid(logit).
+ * Same idx / vals / ws contract as csa_index_topk.
+ */
+csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int32_t* idx,
+                                      float* vals, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_INDEX_H */

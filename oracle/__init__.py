@@ -1,0 +1,277 @@
+"""fp64 CPU oracle of the CSA indexer (ctypes binding of csa_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: tests/, the smoke check and the CPU-baseline leg of
+the benchmark use it. The product package never imports this module, and this
+module imports nothing from the product package.
+
+What it computes (FlashMemory-DeepSeek-V4, "Retriever architecture" and
+"compressed_k format"; "Two-level recall algorithm", Level 2):
+    k      = e4m3(record[:128]) * fp32(record[128:132])
+    logit  = sum_h relu(k . q_h) * fused_w_h
+    score  = sigmoid(logit)
+and the top-k records of each query by (logit desc, position asc).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libcsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PAGE_OOB = 1
+RESIDENT_OOB = 2
+BAD_REQUEST = 16
+LEN_OOB = 32
+
+
+def build(force: bool = False) -> str:
+    """Compiles csa_oracle.c into oracle/libcsa_oracle.so (gcc, OpenMP)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
+           "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("w", ctypes.c_void_p),
+        ("num_q", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("D", ctypes.c_int32),
+        ("kv", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int64),
+        ("page_stride", ctypes.c_int64),
+        ("page_table", ctypes.c_void_p),
+        ("num_req", ctypes.c_int32),
+        ("pt_stride", ctypes.c_int32),
+        ("q_req", ctypes.c_void_p),
+        ("q_len", ctypes.c_void_p),
+        ("resident", ctypes.c_void_p),
+        ("n_resident", ctypes.c_void_p),
+        ("res_stride", ctypes.c_int32),
+    ]
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(_Problem)
+    lib.oracle_e4m3.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3.restype = ctypes.c_double
+    lib.oracle_bf16.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16.restype = ctypes.c_double
+    lib.oracle_scale.argtypes = [ctypes.c_void_p]
+    lib.oracle_scale.restype = ctypes.c_double
+    lib.oracle_sigmoid.argtypes = [ctypes.c_double]
+    lib.oracle_sigmoid.restype = ctypes.c_double
+    lib.oracle_logit.argtypes = [P, ctypes.c_int32, ctypes.c_int64]
+    lib.oracle_logit.restype = ctypes.c_double
+    lib.oracle_visible.argtypes = [P, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p]
+    lib.oracle_visible.restype = ctypes.c_int64
+    lib.oracle_logits.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+    lib.oracle_logits.restype = ctypes.c_int32
+    lib.oracle_topk.argtypes = [P, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p]
+    lib.oracle_topk.restype = ctypes.c_int32
+    lib.oracle_topk_sample.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_topk_sample.restype = ctypes.c_int64
+    lib.oracle_threads.argtypes = []
+    lib.oracle_threads.restype = ctypes.c_int32
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB_PATH)
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+class Problem:
+    """Keeps the host arrays alive and exposes them to the C oracle.
+
+    Takes any object with the attributes of a synthetic workload: q (uint16 bf16
+    bits [num_q, H, D]), fused_w, kv ([num_pages, page_stride] uint8),
+    page_table, q_len, q_req, resident, n_resident.
+    """
+
+    def __init__(self, w):
+        c = np.ascontiguousarray
+        self.q = c(w.q, dtype=np.uint16)
+        self.fused_w = c(w.fused_w, dtype=np.float32)
+        self.kv = c(w.kv, dtype=np.uint8)
+        self.page_table = c(w.page_table, dtype=np.int32)
+        self.q_len = c(w.q_len, dtype=np.int32)
+        self.q_req = None if w.q_req is None else c(w.q_req, dtype=np.int32)
+        self.resident = None if w.resident is None else c(w.resident, dtype=np.int32)
+        self.n_resident = None if w.n_resident is None else c(w.n_resident, dtype=np.int32)
+        self.num_q, self.H, self.D = (int(x) for x in self.q.shape)
+        self.num_req, self.pt_stride = (int(x) for x in self.page_table.shape)
+        self.res_stride = 0 if self.resident is None else int(self.resident.shape[1])
+        self._s = _Problem(
+            _ptr(self.q), _ptr(self.fused_w), self.num_q, self.H, self.D,
+            _ptr(self.kv), int(self.kv.shape[0]), int(self.kv.shape[1]),
+            _ptr(self.page_table), self.num_req, self.pt_stride,
+            _ptr(self.q_req), _ptr(self.q_len), _ptr(self.resident), _ptr(self.n_resident),
+            self.res_stride)
+
+    @property
+    def ref(self):
+        return ctypes.byref(self._s)
+
+    def score_stride(self) -> int:
+        return 64 * max(self.res_stride if self.resident is not None else self.pt_stride, 1)
+
+
+class Oracle:
+    """The oracle's entry points bound to one build of csa_oracle.c."""
+
+    def __init__(self, lib=None):
+        self._lib = lib
+
+    @property
+    def lib(self):
+        return self._lib if self._lib is not None else _load()
+
+    def e4m3(self, byte: int) -> float:
+        return self.lib.oracle_e4m3(int(byte) & 0xFF)
+
+    def bf16(self, bits: int) -> float:
+        return self.lib.oracle_bf16(int(bits) & 0xFFFF)
+
+    def scale(self, record: np.ndarray) -> float:
+        rec = np.ascontiguousarray(record, dtype=np.uint8)
+        return self.lib.oracle_scale(rec.ctypes.data)
+
+    def sigmoid(self, x: float) -> float:
+        return self.lib.oracle_sigmoid(float(x))
+
+    def logit(self, problem: Problem, b: int, position: int) -> float:
+        return self.lib.oracle_logit(problem.ref, int(b), int(position))
+
+    def visible(self, problem: Problem, b: int):
+        return _visible(self.lib, problem, b)
+
+    def logits(self, problem: Problem, stride: int | None = None):
+        return _logits(self.lib, problem, stride)
+
+    def scores(self, problem: Problem, stride: int | None = None):
+        return _scores(self.lib, problem, stride)
+
+    def topk(self, problem: Problem, k: int):
+        return _topk(self.lib, problem, k)
+
+
+def load_build(path: str) -> Oracle:
+    """An Oracle bound to another build of csa_oracle.c (used by mutation tests)."""
+    return Oracle(_bind(path))
+
+
+def e4m3(byte: int) -> float:
+    return Oracle().e4m3(byte)
+
+
+def bf16(bits: int) -> float:
+    return Oracle().bf16(bits)
+
+
+def scale(record: np.ndarray) -> float:
+    return Oracle().scale(record)
+
+
+def sigmoid(x: float) -> float:
+    return Oracle().sigmoid(x)
+
+
+def logit(problem: Problem, b: int, position: int) -> float:
+    return Oracle().logit(problem, b, position)
+
+
+def visible(problem: Problem, b: int):
+    """(positions, columns, flags) of the visible records of row b."""
+    return _visible(_load(), problem, b)
+
+
+def _visible(lib, problem: Problem, b: int):
+    flags = ctypes.c_int32(0)
+    n = lib.oracle_visible(problem.ref, int(b), None, None, ctypes.byref(flags))
+    pos = np.zeros(max(n, 1), dtype=np.int64)
+    col = np.zeros(max(n, 1), dtype=np.int64)
+    lib.oracle_visible(problem.ref, int(b), pos.ctypes.data, col.ctypes.data, None)
+    return pos[:n], col[:n], int(flags.value)
+
+
+def logits(problem: Problem, stride: int | None = None):
+    """(logits [num_q, stride] fp64 (NaN where invisible), valid mask, flags)."""
+    return _logits(_load(), problem, stride)
+
+
+def _logits(lib, problem: Problem, stride: int | None = None):
+    stride = stride or problem.score_stride()
+    out = np.full((problem.num_q, stride), np.nan, dtype=np.float64)
+    valid = np.zeros((problem.num_q, stride), dtype=np.uint8)
+    flags = lib.oracle_logits(problem.ref, out.ctypes.data, valid.ctypes.data, int(stride))
+    return out, valid.astype(bool), int(flags)
+
+
+def scores(problem: Problem, stride: int | None = None):
+    """(scores [num_q, stride] fp64 (NaN where invisible), valid mask, flags)."""
+    return _scores(_load(), problem, stride)
+
+
+def _scores(lib, problem: Problem, stride: int | None = None):
+    lg, valid, flags = _logits(lib, problem, stride)
+    with np.errstate(over="ignore"):
+        sc = 1.0 / (1.0 + np.exp(-lg))
+    return sc, valid, flags
+
+
+def topk(problem: Problem, k: int):
+    """(idx int32 [num_q, k], score fp64, logit fp64, flags) by (logit desc, position asc)."""
+    return _topk(_load(), problem, k)
+
+
+def _topk(lib, problem: Problem, k: int):
+    idx = np.zeros((problem.num_q, k), dtype=np.int32)
+    sc = np.zeros((problem.num_q, k), dtype=np.float64)
+    lg = np.zeros((problem.num_q, k), dtype=np.float64)
+    flags = lib.oracle_topk(problem.ref, int(k), idx.ctypes.data, sc.ctypes.data, lg.ctypes.data)
+    return idx, sc, lg, int(flags)
+
+
+def topk_sample(problem: Problem, b0: int, b1: int, max_records: int, k: int):
+    """Top-k of rows [b0, b1) over at most max_records visible records each.
+
+    Returns (idx, score, records scored). Used to time the oracle on a bounded
+    sample of a large workload.
+    """
+    n = b1 - b0
+    idx = np.zeros((n, k), dtype=np.int32)
+    sc = np.zeros((n, k), dtype=np.float64)
+    scored = _load().oracle_topk_sample(problem.ref, int(b0), int(b1), int(max_records), int(k),
+                                        idx.ctypes.data, sc.ctypes.data)
+    return idx, sc, int(scored)
+
+
+def threads() -> int:
+    return int(_load().oracle_threads())

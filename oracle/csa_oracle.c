@@ -1,0 +1,354 @@
+/*
+ * csa_oracle.c — plain fp64 CPU oracle of the CSA indexer.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
+ * this file: only tests/, the smoke check and the CPU-baseline leg of the
+ * benchmark do. It shares no code, header, table or constant with the CUDA
+ * library; the two only see the same seeded input bytes.
+ *
+ * Every function restates one step of the method as the pages define it:
+ *
+ *   FlashMemory-DeepSeek-V4, "compressed_k format": a record is HEAD_DIM e4m3
+ *     bytes followed by a 4-byte fp32 scale; k = e4m3(bytes) * scale.
+ *   FlashMemory-DeepSeek-V4, "Retriever architecture":
+ *     score = sigmoid( sum_heads( relu(k . q_h) * fused_w_h ) ), in [0, 1].
+ *   FlashMemory-DeepSeek-V4, "Two-level recall algorithm", Level 2: keep the
+ *     top-512 per query, over the full history or confined to the resident set
+ *     (non-resident logits set to -inf, i.e. left out).
+ *   BatchGen #153 commit log: relu is applied before the head-weighted sum;
+ *     lengths count compressed records.
+ *
+ * Readings where the pages are silent (each also listed in the design doc):
+ *   - e4m3 is the OCP "fn" variant (bias 7, no infinities, S.1111.111 = NaN).
+ *   - The trailing scale is little-endian IEEE binary32.
+ *   - All arithmetic is fp64 (the pages' `.float()` dequant rounds k to fp32,
+ *     a relative change below 6e-8, far inside the tolerance).
+ *   - Ties in the logit are broken by the lower logical position.
+ *   - Fewer than k visible records: the tail is idx -1, score 0 (sigmoid(-inf)).
+ *   - Invalid geometry (page id out of range, resident page past the length,
+ *     request id out of range) drops the affected records and sets a flag bit.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.
+ * -ffp-contract=off keeps the result identical on x86 and Arm.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_D 128
+#define OR_PAGE 64
+#define OR_REC_BYTES (OR_D + 4)
+
+/* Flag bits reported by the oracle (the oracle's own numbering). */
+#define OR_FLAG_PAGE_OOB 1
+#define OR_FLAG_RESIDENT_OOB 2
+#define OR_FLAG_BAD_REQUEST 16
+#define OR_FLAG_LEN_OOB 32
+
+/* Host-side description of one indexer problem (the oracle's own type). */
+typedef struct oracle_problem {
+  const uint16_t* q;          /* [num_q, H, D] bf16 bit patterns */
+  const float* w;             /* [num_q, H] */
+  int32_t num_q, H, D;
+  const uint8_t* kv;          /* page p at kv + p * page_stride */
+  int64_t num_pages, page_stride;
+  const int32_t* page_table;  /* [num_req, pt_stride] */
+  int32_t num_req, pt_stride;
+  const int32_t* q_req;       /* NULL = identity */
+  const int32_t* q_len;
+  const int32_t* resident;    /* NULL = full history */
+  const int32_t* n_resident;
+  int32_t res_stride;
+} oracle_problem;
+
+/* OCP FP8 E4M3 ("fn") byte -> value. E = 0: subnormal m/8 * 2^-6; otherwise
+ * (1 + m/8) * 2^(E-7); E = 15 and m = 7 is NaN. */
+double oracle_e4m3(uint8_t b) {
+  int sign = b >> 7;
+  int E = (b >> 3) & 15;
+  int m = b & 7;
+  double v;
+  if (E == 15 && m == 7) return NAN;
+  if (E == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, E - 7);
+  return sign ? -v : v;
+}
+
+/* bf16 bit pattern -> value: the upper half of an IEEE binary32. */
+double oracle_bf16(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Trailing scale: bytes 128..131 of the record, little-endian binary32. */
+double oracle_scale(const uint8_t* rec) {
+  uint32_t u = (uint32_t)rec[OR_D] | ((uint32_t)rec[OR_D + 1] << 8) |
+               ((uint32_t)rec[OR_D + 2] << 16) | ((uint32_t)rec[OR_D + 3] << 24);
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Request of query row b, or -1 when out of range. */
+static int32_t row_request(const oracle_problem* P, int32_t b, int32_t* flags) {
+  int32_t req = P->q_req ? P->q_req[b] : b;
+  if (req < 0 || req >= P->num_req) {
+    *flags |= OR_FLAG_BAD_REQUEST;
+    return -1;
+  }
+  return req;
+}
+
+/* Visible length of row b in records: q_len clamped to [0, 64 * pt_stride]. */
+static int64_t row_length(const oracle_problem* P, int32_t b, int32_t* flags) {
+  int64_t L = P->q_len[b];
+  if (L < 0) {
+    *flags |= OR_FLAG_LEN_OOB;
+    L = 0;
+  }
+  if (L > (int64_t)OR_PAGE * P->pt_stride) {
+    *flags |= OR_FLAG_LEN_OOB;
+    L = (int64_t)OR_PAGE * P->pt_stride;
+  }
+  return L;
+}
+
+/*
+ * Lists the visible records of row b: their logical positions and the score
+ * column each one occupies (full mode: column = position; resident mode:
+ * column = j*64 + r for the j-th listed page). Returns the count; `pos` and
+ * `col` may be NULL to count only.
+ */
+int64_t oracle_visible(const oracle_problem* P, int32_t b, int64_t* pos, int64_t* col,
+                       int32_t* flags_out) {
+  int32_t flags = 0;
+  int64_t n = 0;
+  int32_t req = row_request(P, b, &flags);
+  if (req >= 0) {
+    int64_t L = row_length(P, b, &flags);
+    int64_t npages = (L + OR_PAGE - 1) / OR_PAGE;
+    if (!P->resident) {
+      for (int64_t p = 0; p < npages; ++p) {
+        int32_t phys = P->page_table[(int64_t)req * P->pt_stride + p];
+        if (phys < 0 || phys >= P->num_pages) {
+          flags |= OR_FLAG_PAGE_OOB;
+          continue;
+        }
+        for (int64_t r = 0; r < OR_PAGE && p * OR_PAGE + r < L; ++r) {
+          if (pos) pos[n] = p * OR_PAGE + r;
+          if (col) col[n] = p * OR_PAGE + r;
+          ++n;
+        }
+      }
+    } else {
+      int64_t nres = P->n_resident[req];
+      if (nres < 0) {
+        flags |= OR_FLAG_LEN_OOB;
+        nres = 0;
+      }
+      if (nres > P->res_stride) {
+        flags |= OR_FLAG_LEN_OOB;
+        nres = P->res_stride;
+      }
+      for (int64_t j = 0; j < nres; ++j) {
+        int64_t p = P->resident[(int64_t)req * P->res_stride + j];
+        if (p < 0 || p >= npages) {
+          flags |= OR_FLAG_RESIDENT_OOB;
+          continue;
+        }
+        int32_t phys = P->page_table[(int64_t)req * P->pt_stride + p];
+        if (phys < 0 || phys >= P->num_pages) {
+          flags |= OR_FLAG_PAGE_OOB;
+          continue;
+        }
+        for (int64_t r = 0; r < OR_PAGE && p * OR_PAGE + r < L; ++r) {
+          if (pos) pos[n] = p * OR_PAGE + r;
+          if (col) col[n] = j * OR_PAGE + r;
+          ++n;
+        }
+      }
+    }
+  }
+  if (flags_out) *flags_out |= flags;
+  return n;
+}
+
+/* q of row b decoded to fp64 and stored d-major: qT[d*H + h] = q[b][h][d]. */
+static void decode_query(const oracle_problem* P, int32_t b, double* qT) {
+  const int H = P->H;
+  const uint16_t* qb = P->q + (int64_t)b * H * OR_D;
+  for (int h = 0; h < H; ++h)
+    for (int d = 0; d < OR_D; ++d) qT[d * H + h] = oracle_bf16(qb[h * OR_D + d]);
+}
+
+/*
+ * logit of row b at a visible logical position, given the row's decoded query:
+ * sum over heads of relu(k . q_h) * w_h, with k the dequantised record.
+ * Each head's dot product is accumulated over d = 0..D-1 in order; the loop
+ * runs d outermost so that all heads advance together, which leaves each
+ * head's summation order unchanged.
+ */
+static double logit_at(const oracle_problem* P, int32_t b, const double* qT, int64_t position) {
+  const int H = P->H;
+  int32_t req = P->q_req ? P->q_req[b] : b;
+  int64_t p = position / OR_PAGE, r = position % OR_PAGE;
+  int32_t phys = P->page_table[(int64_t)req * P->pt_stride + p];
+  const uint8_t* rec = P->kv + (int64_t)phys * P->page_stride + r * OR_REC_BYTES;
+  const double s = oracle_scale(rec);
+  double dot[256];
+  for (int h = 0; h < H; ++h) dot[h] = 0.0;
+  for (int d = 0; d < OR_D; ++d) {
+    const double kd = oracle_e4m3(rec[d]) * s; /* dequantise: e4m3 value times scale */
+    const double* qd = qT + d * H;
+    for (int h = 0; h < H; ++h) dot[h] += kd * qd[h];
+  }
+  double logit = 0.0;
+  for (int h = 0; h < H; ++h) {
+    const double relu = dot[h] > 0.0 ? dot[h] : 0.0; /* relu before the weighted sum */
+    logit += relu * (double)P->w[(int64_t)b * H + h];
+  }
+  return logit;
+}
+
+/* logit of row b at one visible logical position (decodes q itself). */
+double oracle_logit(const oracle_problem* P, int32_t b, int64_t position) {
+  double* qT = (double*)malloc(sizeof(double) * OR_D * P->H);
+  decode_query(P, b, qT);
+  double v = logit_at(P, b, qT, position);
+  free(qT);
+  return v;
+}
+
+double oracle_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/*
+ * Logits of every visible record, in score-matrix layout: out[b*stride + col].
+ * Invisible columns are left untouched; valid[b*stride + col] is set to 1 for
+ * written columns (valid may be NULL). Returns the OR of the flag bits.
+ */
+int32_t oracle_logits(const oracle_problem* P, double* out, uint8_t* valid, int64_t stride) {
+  int32_t flags = 0;
+  for (int32_t b = 0; b < P->num_q; ++b) {
+    int64_t n = oracle_visible(P, b, NULL, NULL, &flags);
+    if (n == 0) continue;
+    int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * n);
+    int64_t* col = (int64_t*)malloc(sizeof(int64_t) * n);
+    oracle_visible(P, b, pos, col, NULL);
+    double* qT = (double*)malloc(sizeof(double) * OR_D * P->H);
+    decode_query(P, b, qT);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+      out[(int64_t)b * stride + col[i]] = logit_at(P, b, qT, pos[i]);
+      if (valid) valid[(int64_t)b * stride + col[i]] = 1;
+    }
+    free(qT);
+    free(pos);
+    free(col);
+  }
+  return flags;
+}
+
+typedef struct {
+  double logit;
+  int64_t pos;
+} ranked;
+
+/* Order: logit descending, then position ascending. */
+static int by_logit_then_position(const void* a, const void* b) {
+  const ranked* x = (const ranked*)a;
+  const ranked* y = (const ranked*)b;
+  if (x->logit > y->logit) return -1;
+  if (x->logit < y->logit) return 1;
+  return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+/*
+ * Top-k of every row: idx[b*k + i] (logical position, -1 padding), score
+ * (sigmoid of the logit, 0 for padding) and logit (-inf for padding).
+ * Any of score / logit may be NULL. Returns the OR of the flag bits.
+ */
+int32_t oracle_topk(const oracle_problem* P, int32_t k, int32_t* idx, double* score,
+                    double* logit) {
+  int32_t flags = 0;
+  for (int32_t b = 0; b < P->num_q; ++b) {
+    int64_t n = oracle_visible(P, b, NULL, NULL, &flags);
+    ranked* all = (ranked*)malloc(sizeof(ranked) * (n > 0 ? n : 1));
+    int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (n > 0 ? n : 1));
+    oracle_visible(P, b, pos, NULL, NULL);
+    double* qT = (double*)malloc(sizeof(double) * OR_D * P->H);
+    decode_query(P, b, qT);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+      all[i].logit = logit_at(P, b, qT, pos[i]);
+      all[i].pos = pos[i];
+    }
+    free(qT);
+    qsort(all, (size_t)n, sizeof(ranked), by_logit_then_position);
+    for (int32_t i = 0; i < k; ++i) {
+      int64_t o = (int64_t)b * k + i;
+      if (i < n) {
+        idx[o] = (int32_t)all[i].pos;
+        if (score) score[o] = oracle_sigmoid(all[i].logit);
+        if (logit) logit[o] = all[i].logit;
+      } else {
+        idx[o] = -1;
+        if (score) score[o] = 0.0;
+        if (logit) logit[o] = -INFINITY;
+      }
+    }
+    free(all);
+    free(pos);
+  }
+  return flags;
+}
+
+/*
+ * Same as oracle_topk for rows [b0, b1) only and for at most `max_records`
+ * visible records per row (the first ones in column order). Used to time the
+ * oracle on a bounded sample of a large workload.
+ */
+int64_t oracle_topk_sample(const oracle_problem* P, int32_t b0, int32_t b1, int64_t max_records,
+                           int32_t k, int32_t* idx, double* score) {
+  int64_t scored = 0;
+  for (int32_t b = b0; b < b1; ++b) {
+    int32_t flags = 0;
+    int64_t n = oracle_visible(P, b, NULL, NULL, &flags);
+    int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (n > 0 ? n : 1));
+    oracle_visible(P, b, pos, NULL, NULL);
+    if (n > max_records) n = max_records;
+    ranked* all = (ranked*)malloc(sizeof(ranked) * (n > 0 ? n : 1));
+    double* qT = (double*)malloc(sizeof(double) * OR_D * P->H);
+    decode_query(P, b, qT);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+      all[i].logit = logit_at(P, b, qT, pos[i]);
+      all[i].pos = pos[i];
+    }
+    free(qT);
+    qsort(all, (size_t)n, sizeof(ranked), by_logit_then_position);
+    for (int32_t i = 0; i < k; ++i) {
+      int64_t o = (int64_t)(b - b0) * k + i;
+      idx[o] = i < n ? (int32_t)all[i].pos : -1;
+      if (score) score[o] = i < n ? oracle_sigmoid(all[i].logit) : 0.0;
+    }
+    scored += n;
+    free(all);
+    free(pos);
+  }
+  return scored;
+}
+
+/* Threads the OpenMP runtime will use (1 when built without OpenMP). */
+int32_t oracle_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,373 @@
+"""Checks that pin the oracle to things other than itself.
+
+Each `pin_*` function takes an `oracle.Oracle` and raises AssertionError when
+the oracle disagrees with an outside fact: a library routine (torch's fp8 and
+bf16 casts, numpy's float64 matmul and lexsort), the format definition, a
+closed form, a hand-worked example or an invariant of the method. The same
+functions run against the real oracle (all must pass) and against builds of
+the oracle with a mistake planted in them (at least one must fail).
+"""
+from __future__ import annotations
+
+import math
+import os
+import struct
+
+import numpy as np
+import torch
+
+from sparse_attention_kv_e4m3_gb300 import synth
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+H, D, PAGE, REC = 64, 128, 64, 132
+
+
+# ---------------------------------------------------------------- helpers
+
+def e4m3_code(x: float) -> int:
+    """The e4m3 byte of x by torch's cast (round to nearest even)."""
+    return int(torch.tensor([x], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).item())
+
+
+def bf16_bits(x) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def hand_workload(records: np.ndarray, q: np.ndarray, w: np.ndarray, q_len=None,
+                  num_q: int = 1) -> synth.Workload:
+    """One request whose history is `records` ([n, 132] uint8), identity pages."""
+    n = records.shape[0]
+    pages = max(1, (n + PAGE - 1) // PAGE)
+    kv = np.zeros((pages, PAGE * REC), dtype=np.uint8)
+    kv.reshape(-1, REC)[:n] = records
+    qb = np.broadcast_to(bf16_bits(q), (num_q, H, D)).copy()
+    wb = np.broadcast_to(np.asarray(w, dtype=np.float32), (num_q, H)).copy()
+    return synth.Workload(
+        name="hand", q=qb, fused_w=wb, kv=kv,
+        page_table=np.arange(pages, dtype=np.int32).reshape(1, pages),
+        q_len=np.full(num_q, n if q_len is None else q_len, dtype=np.int32),
+        q_req=np.zeros(num_q, dtype=np.int32))
+
+
+def record(values: dict, scale: float) -> np.ndarray:
+    """A 132-byte record: e4m3 bytes given as {d: byte}, then the fp32 scale."""
+    r = np.zeros(REC, dtype=np.uint8)
+    for d, b in values.items():
+        r[d] = b
+    r[D:] = np.frombuffer(struct.pack("<f", scale), dtype=np.uint8)
+    return r
+
+
+def tiny_workloads():
+    """Small seeded workloads spanning partial pages, shuffled pages, several rows,
+    resident subsets and shared-request rows."""
+    yield synth.make_workload("t_full", num_q=3, history=[130, 70, 1], seed=11)
+    yield synth.make_workload("t_out", num_q=2, history=[200, 64], outlier_frac=0.2, seed=12)
+    yield synth.make_workload("t_res", num_q=2, history=[600, 333], resident_pages=3, seed=13)
+    yield synth.make_workload("t_pre", num_q=5, history=[300], single_request=True,
+                              q_len=lambda h, n: np.array([1, 64, 65, 250, 300]), seed=14)
+    yield synth.make_workload("t_pad", num_q=2, history=[100, 129], page_pad=48, seed=15)
+
+
+def brute_logits(w: synth.Workload):
+    """Independent float64 restatement with library primitives: torch's e4m3 and
+    bf16 decodes, numpy's matmul. Returns {(b, position): (logit, column)}."""
+    table = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    table = table.to(torch.float64).numpy()
+    out = {}
+    for b in range(w.num_q):
+        req = int(w.q_req[b]) if w.q_req is not None else b
+        L = min(max(int(w.q_len[b]), 0), PAGE * w.pt_stride)
+        qf = torch.from_numpy(w.q[b].view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+        wf = w.fused_w[b].astype(np.float64)
+        npages = (L + PAGE - 1) // PAGE
+        if w.resident is None:
+            plist = [(p, p) for p in range(npages)]
+        else:
+            plist = [(int(p), j) for j, p in enumerate(w.resident[req, : int(w.n_resident[req])])]
+        for p, j in plist:
+            if not (0 <= p < npages):
+                continue
+            phys = int(w.page_table[req, p])
+            if not (0 <= phys < w.num_pages):
+                continue
+            for r in range(PAGE):
+                pos = p * PAGE + r
+                if pos >= L:
+                    break
+                rec = w.kv[phys, r * REC:(r + 1) * REC]
+                s = float(np.frombuffer(rec[D:].tobytes(), dtype="<f4")[0])
+                k = table[rec[:D]] * s
+                dots = qf @ k
+                logit = float(np.maximum(dots, 0.0) @ wf)
+                out[(b, pos)] = (logit, j * PAGE + r)
+    return out
+
+
+def brute_topk(w: synth.Workload, k: int):
+    lg = brute_logits(w)
+    idx = np.full((w.num_q, k), -1, dtype=np.int64)
+    val = np.full((w.num_q, k), -np.inf)
+    for b in range(w.num_q):
+        items = [(pos, v[0]) for (bb, pos), v in lg.items() if bb == b]
+        if not items:
+            continue
+        pos = np.array([i[0] for i in items])
+        lv = np.array([i[1] for i in items])
+        order = np.lexsort((pos, -lv))[:k]
+        idx[b, : len(order)] = pos[order]
+        val[b, : len(order)] = lv[order]
+    return idx, val
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_e4m3_vs_torch(o: O.Oracle):
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    for b in range(256):
+        got, want = o.e4m3(b), float(lib[b])
+        if math.isnan(want):
+            assert math.isnan(got), f"byte {b:#04x}: want NaN, got {got}"
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), \
+                f"byte {b:#04x}: {got} != {want}"
+
+
+def pin_e4m3_spec_golden(o: O.Oracle):
+    with open(os.path.join(GOLDEN, "e4m3_ocp_values.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if not line:
+                continue
+            b, v = int(line[0], 16), float(line[1])
+            got = o.e4m3(b)
+            if math.isnan(v):
+                assert math.isnan(got), f"{b:#04x}"
+            else:
+                assert got == v and math.copysign(1, got) == math.copysign(1, v), f"{b:#04x}: {got} != {v}"
+
+
+def pin_bf16_vs_torch(o: O.Oracle):
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 1 << 16, size=4000).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]  # finite values only
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([o.bf16(int(x)) for x in bits])
+    assert np.array_equal(got, want)
+
+
+def pin_scale_little_endian(o: O.Oracle):
+    for s in (2.5, -0.75, 1e-3, 3.0e5):
+        r = record({}, s)
+        assert o.scale(r) == struct.unpack("<f", struct.pack("<f", s))[0]
+
+
+def pin_sigmoid_closed_form(o: O.Oracle):
+    assert o.sigmoid(0.0) == 0.5
+    assert abs(o.sigmoid(math.log(3.0)) - 0.75) < 1e-15
+    assert abs(o.sigmoid(-math.log(3.0)) - 0.25) < 1e-15
+
+
+def pin_worked_example(o: O.Oracle):
+    vals = {}
+    with open(os.path.join(GOLDEN, "worked_example.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if line:
+                vals[line[0]] = line[1:]
+    rec = record({d: int(x, 16) for d, x in enumerate(vals["bytes"])}, float(vals["scale"][0]))
+    q = np.zeros((H, D), dtype=np.float32)
+    for h in range(3):
+        q[h, :3] = [float(x) for x in vals[f"q{h}"]]
+    w = np.zeros(H, dtype=np.float32)
+    w[:3] = [float(x) for x in vals["w"]]
+    P = O.Problem(hand_workload(rec[None, :], q, w))
+    lg = o.logit(P, 0, 0)
+    assert lg == float(vals["logit"][0]), lg
+    idx, sc, lgk, _ = o.topk(P, 4)
+    assert idx[0, 0] == 0 and list(idx[0, 1:]) == [-1, -1, -1]
+    assert abs(sc[0, 0] - float(vals["score"][0])) < 1e-15
+    assert list(sc[0, 1:]) == [0.0, 0.0, 0.0]
+
+
+def pin_zero_weights_half(o: O.Oracle):
+    w = synth.make_workload("zw", num_q=2, history=[150, 90], seed=3)
+    w.fused_w[:] = 0.0
+    P = O.Problem(w)
+    sc, valid, _ = o.scores(P)
+    assert valid.sum() == 240 and np.all(sc[valid] == 0.5)
+    idx, s, _, _ = o.topk(P, 100)
+    # equal logits everywhere: the lower position wins every tie
+    assert np.array_equal(idx[0], np.arange(100)) and np.array_equal(idx[1], np.arange(90).tolist() + [-1] * 10)
+    assert np.all(s[0] == 0.5)
+
+
+def pin_zero_query_half(o: O.Oracle):
+    w = synth.make_workload("zq", num_q=1, history=[70], seed=4)
+    w.q[:] = 0
+    sc, valid, _ = o.scores(O.Problem(w))
+    assert np.all(sc[valid] == 0.5)
+
+
+def pin_one_hot(o: O.Oracle):
+    """One head, w = 1, q one-hot at d0: score = sigmoid(max(0, s * e4m3(byte[d0])))."""
+    w = synth.make_workload("oh", num_q=1, history=[128], seed=5)
+    d0 = 37
+    q = np.zeros((H, D), dtype=np.float32)
+    q[9, d0] = 1.0
+    w.q[0] = bf16_bits(q)
+    w.fused_w[0] = 0.0
+    w.fused_w[0, 9] = 1.0
+    P = O.Problem(w)
+    table = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for pos in (0, 5, 63, 64, 127):
+        phys = int(w.page_table[0, pos // PAGE])
+        rec = w.kv[phys, (pos % PAGE) * REC:(pos % PAGE + 1) * REC]
+        s = float(np.frombuffer(rec[D:].tobytes(), dtype="<f4")[0])
+        want = max(0.0, s * table[rec[d0]])
+        assert o.logit(P, 0, pos) == want
+
+
+def pin_relu_before_sum(o: O.Oracle):
+    """relu comes before the head-weighted sum (BatchGen #153 commit log): record A
+    has head dots (+3, -5), record B (+1, +1); with w = (1, 1) A scores 3 and B 2,
+    so A ranks first; summing before relu would rank B first (-2 < 2)."""
+    q = np.zeros((H, D), dtype=np.float32)
+    q[0, 0] = 1.0
+    q[1, 1] = 1.0
+    w = np.zeros(H, dtype=np.float32)
+    w[:2] = 1.0
+    A = record({0: e4m3_code(3.0), 1: e4m3_code(-5.0)}, 1.0)
+    B = record({0: e4m3_code(1.0), 1: e4m3_code(1.0)}, 1.0)
+    P = O.Problem(hand_workload(np.stack([B, A]), q, w))
+    assert o.logit(P, 0, 0) == 2.0 and o.logit(P, 0, 1) == 3.0
+    idx, _, _, _ = o.topk(P, 1)
+    assert idx[0, 0] == 1
+
+
+def pin_negative_scale(o: O.Oracle):
+    """relu acts on the dequantised k . q, so a negative scale flips which heads pass:
+    x = (+3, -5), s = -1 -> relu(s*x) = (0, 5) -> logit 5 with w = (1, 1)."""
+    q = np.zeros((H, D), dtype=np.float32)
+    q[0, 0] = 1.0
+    q[1, 1] = 1.0
+    w = np.zeros(H, dtype=np.float32)
+    w[:2] = 1.0
+    A = record({0: e4m3_code(3.0), 1: e4m3_code(-5.0)}, -1.0)
+    P = O.Problem(hand_workload(A[None, :], q, w))
+    assert o.logit(P, 0, 0) == 5.0
+
+
+def pin_padding(o: O.Oracle):
+    w = synth.make_workload("pad", num_q=2, history=[10, 0], seed=6)
+    idx, sc, lg, _ = o.topk(O.Problem(w), 16)
+    assert np.all(idx[0, 10:] == -1) and np.all(sc[0, 10:] == 0.0) and np.all(np.isneginf(lg[0, 10:]))
+    assert sorted(idx[0, :10]) == list(range(10))
+    assert np.all(idx[1] == -1) and np.all(sc[1] == 0.0)
+
+
+def pin_brute_force(o: O.Oracle):
+    for w in tiny_workloads():
+        P = O.Problem(w)
+        want = brute_logits(w)
+        lg, valid, flags = o.logits(P)
+        assert flags == 0, (w.name, flags)
+        assert int(valid.sum()) == len(want), (w.name, int(valid.sum()), len(want))
+        for (b, pos), (v, col) in want.items():
+            assert valid[b, col], (w.name, b, pos)
+            assert abs(lg[b, col] - v) <= 1e-12 * (1.0 + abs(v)), (w.name, b, pos, lg[b, col], v)
+        k = 40
+        bi, bv = brute_topk(w, k)
+        idx, sc, lgk, _ = o.topk(P, k)
+        assert np.array_equal(idx, bi), w.name
+        fin = np.isfinite(bv)
+        assert np.allclose(lgk[fin], bv[fin], rtol=1e-12, atol=1e-12)
+        with np.errstate(over="ignore"):
+            assert np.allclose(sc[fin], 1.0 / (1.0 + np.exp(-bv[fin])), rtol=1e-12, atol=1e-15)
+
+
+def pin_scores_in_unit_interval(o: O.Oracle):
+    w = synth.make_workload("u", num_q=2, history=[300, 77], outlier_frac=0.3, seed=7)
+    sc, valid, _ = o.scores(O.Problem(w))
+    assert np.all((sc[valid] >= 0.0) & (sc[valid] <= 1.0))
+
+
+def pin_resident_is_masked_full(o: O.Oracle):
+    """Resident mode = full mode with non-resident logits at -inf
+    ("Two-level recall algorithm", Level 2)."""
+    w = synth.make_workload("rm", num_q=2, history=[700, 450], resident_pages=4, seed=8)
+    k = 50
+    idx_r, sc_r, _, _ = o.topk(O.Problem(w), k)
+    full = synth.Workload(name="rf", q=w.q, fused_w=w.fused_w, kv=w.kv, page_table=w.page_table,
+                          q_len=w.q_len)
+    lg, valid, _ = o.logits(O.Problem(full))
+    for b in range(2):
+        pages = set(int(p) for p in w.resident[b, : int(w.n_resident[b])])
+        pos = np.array([n for n in range(int(w.q_len[b])) if n // PAGE in pages])
+        order = np.lexsort((pos, -lg[b, pos]))[:k]
+        want = np.full(k, -1)
+        want[: len(order)] = pos[order]
+        assert np.array_equal(idx_r[b], want), b
+
+
+def pin_physical_relayout(o: O.Oracle):
+    """Moving pages to other physical slots (and updating the page table) changes nothing."""
+    w = synth.make_workload("pr", num_q=2, history=[256, 190], seed=9)
+    idx0, sc0, _, _ = o.topk(O.Problem(w), 64)
+    perm = np.random.default_rng(2).permutation(w.num_pages)
+    kv2 = np.empty_like(w.kv)
+    kv2[perm] = w.kv
+    w2 = synth.Workload(name="pr2", q=w.q, fused_w=w.fused_w, kv=kv2, page_table=perm[w.page_table].astype(np.int32),
+                        q_len=w.q_len)
+    idx1, sc1, _, _ = o.topk(O.Problem(w2), 64)
+    assert np.array_equal(idx0, idx1) and np.array_equal(sc0, sc1)
+
+
+def pin_logical_permutation(o: O.Oracle):
+    """Permuting a request's logical pages permutes the returned positions."""
+    w = synth.make_workload("lp", num_q=1, history=[320], seed=10)
+    idx0, sc0, _, _ = o.topk(O.Problem(w), 80)
+    pi = np.array([3, 0, 4, 1, 2])  # new logical page p reads old logical page pi[p]
+    w2 = synth.Workload(name="lp2", q=w.q, fused_w=w.fused_w, kv=w.kv,
+                        page_table=w.page_table[:, pi].copy(), q_len=w.q_len)
+    idx1, sc1, _, _ = o.topk(O.Problem(w2), 80)
+    inv = np.argsort(pi)
+    mapped = inv[idx0[0] // PAGE] * PAGE + idx0[0] % PAGE
+    assert np.array_equal(np.sort(mapped), np.sort(idx1[0])) and np.array_equal(sc0, sc1)
+
+
+def pin_positive_rescaling(o: O.Oracle):
+    """Scaling every fused_w by c > 0, or every record scale by c > 0 when w >= 0,
+    keeps the top-k (sigmoid and relu are monotone / positively homogeneous)."""
+    w = synth.make_workload("sc", num_q=2, history=[260, 140], seed=16)
+    idx0, _, _, _ = o.topk(O.Problem(w), 60)
+    w.fused_w *= np.float32(4.0)
+    idx1, _, _, _ = o.topk(O.Problem(w), 60)
+    assert np.array_equal(idx0, idx1)
+    w.fused_w[:] = np.abs(w.fused_w)
+    idx2, _, _, _ = o.topk(O.Problem(w), 60)
+    recs = w.kv[:, : PAGE * REC].reshape(-1, REC)
+    sc = recs[:, D:].copy().view("<f4") * np.float32(8.0)
+    recs[:, D:] = sc.view(np.uint8)
+    idx3, _, _, _ = o.topk(O.Problem(w), 60)
+    assert np.array_equal(idx2, idx3)
+
+
+def pin_invalid_geometry(o: O.Oracle):
+    w = synth.make_workload("bad", num_q=3, history=[200, 200, 200], seed=17)
+    w.page_table[0, 1] = w.num_pages + 5        # page 1 of row 0 out of range
+    w.q_req = np.array([0, 1, 7], dtype=np.int32)  # row 2 names a missing request
+    P = O.Problem(w)
+    pos0, _, f0 = o.visible(P, 0)
+    assert f0 & O.PAGE_OOB and len(pos0) == 200 - 64 and not np.any((pos0 >= 64) & (pos0 < 128))
+    pos2, _, f2 = o.visible(P, 2)
+    assert f2 & O.BAD_REQUEST and len(pos2) == 0
+    r = synth.make_workload("badr", num_q=1, history=[300], resident_pages=2, seed=18)
+    r.resident[0, 1] = 5                         # == ceil(300/64): first page past the end
+    posr, _, fr = o.visible(O.Problem(r), 0)
+    assert fr & O.RESIDENT_OOB and len(posr) == min(64, 300 - 64 * int(r.resident[0, 0]))
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

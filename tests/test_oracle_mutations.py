@@ -1,0 +1,71 @@
+"""Plants one plausible mistake at a time in a copy of the oracle's C source and
+checks that the pin battery rejects every such build."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle as O
+
+SRC = os.path.join(os.path.dirname(O.__file__), "csa_oracle.c")
+
+MUTATIONS = [
+    ("relu_dropped", "const double relu = dot[h] > 0.0 ? dot[h] : 0.0;", "const double relu = dot[h];"),
+    ("weight_dropped", "logit += relu * (double)P->w[(int64_t)b * H + h];", "logit += relu;"),
+    ("weight_of_row0", "logit += relu * (double)P->w[(int64_t)b * H + h];", "logit += relu * (double)P->w[h];"),
+    ("e4m3_bias_8", "v = ldexp(1.0 + (double)m / 8.0, E - 7);", "v = ldexp(1.0 + (double)m / 8.0, E - 8);"),
+    ("e4m3_subnormal_exp", "v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    ("e4m3_nan_all_E15", "if (E == 15 && m == 7) return NAN;", "if (E == 15) return NAN;"),
+    ("e4m3_sign_dropped", "return sign ? -v : v;", "return v;"),
+    ("scale_ignored", "const double kd = oracle_e4m3(rec[d]) * s;", "const double kd = oracle_e4m3(rec[d]);"),
+    ("scale_big_endian",
+     "uint32_t u = (uint32_t)rec[OR_D] | ((uint32_t)rec[OR_D + 1] << 8) |\n               ((uint32_t)rec[OR_D + 2] << 16) | ((uint32_t)rec[OR_D + 3] << 24);",
+     "uint32_t u = (uint32_t)rec[OR_D + 3] | ((uint32_t)rec[OR_D + 2] << 8) |\n               ((uint32_t)rec[OR_D + 1] << 16) | ((uint32_t)rec[OR_D] << 24);"),
+    ("q_transposed", "qT[d * H + h] = oracle_bf16(qb[h * OR_D + d]);", "qT[d * H + h] = oracle_bf16(qb[d * H + h]);"),
+    ("bf16_low_half", "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
+    ("tie_break_reversed", "return (x->pos > y->pos) - (x->pos < y->pos);", "return (x->pos < y->pos) - (x->pos > y->pos);"),
+    ("length_off_by_one",
+     "for (int64_t r = 0; r < OR_PAGE && p * OR_PAGE + r < L; ++r) {\n          if (pos) pos[n] = p * OR_PAGE + r;\n          if (col) col[n] = p * OR_PAGE + r;",
+     "for (int64_t r = 0; r < OR_PAGE && p * OR_PAGE + r <= L; ++r) {\n          if (pos) pos[n] = p * OR_PAGE + r;\n          if (col) col[n] = p * OR_PAGE + r;"),
+    ("resident_column_is_position", "if (col) col[n] = j * OR_PAGE + r;", "if (col) col[n] = p * OR_PAGE + r;"),
+    ("page_table_ignored", "int32_t phys = P->page_table[(int64_t)req * P->pt_stride + p];\n  const uint8_t* rec",
+     "int32_t phys = (int32_t)p;\n  const uint8_t* rec"),
+    ("sigmoid_sign", "return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));"),
+    ("padding_score_half", "if (score) score[o] = 0.0;\n        if (logit) logit[o] = -INFINITY;",
+     "if (score) score[o] = 0.5;\n        if (logit) logit[o] = -INFINITY;"),
+    ("resident_bound_off", "if (p < 0 || p >= npages) {", "if (p < 0 || p > npages) {"),
+    ("bad_request_kept", "if (req < 0 || req >= P->num_req) {", "if (req < 0) {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"lib{name}.so"
+    c.write_text(src.replace(old, new, 1))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    # The battery runs in a child process: a mutant may also crash outright (an
+    # out-of-range write), which counts as caught as well.
+    r = subprocess.run([sys.executable, "-c", _RUNNER, str(so)], capture_output=True, text=True,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))), timeout=600)
+    assert r.returncode != 0, f"no pin rejects the planted mistake '{name}':\n{r.stdout}{r.stderr}"
+    assert r.returncode == 3 or r.returncode < 0, r.stderr
+
+
+_RUNNER = """
+import sys
+sys.path[:0] = ['.', 'tests']
+import _pins, oracle as O
+o = O.load_build(sys.argv[1])
+for pin in _pins.ALL_PINS:
+    try:
+        pin(o)
+    except AssertionError:
+        print('caught by', pin.__name__)
+        sys.exit(3)
+sys.exit(0)
+"""
