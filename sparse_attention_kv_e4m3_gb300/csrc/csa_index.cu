@@ -1,0 +1,1099 @@
+// csa_index.cu — the CSA indexer hot path on GB300 (sm_103a) and its C ABI.
+//
+// What is computed (FlashMemory-DeepSeek-V4, "Retriever architecture",
+// "compressed_k format", "Two-level recall algorithm"):
+//   k_n      = e4m3(record_n[0:128]) * fp32(record_n[128:132])
+//   logit_bn = sum_h relu(k_n . q_b[h]) * fused_w_b[h]
+//   score_bn = sigmoid(logit_bn)
+// and the top-k records of each query row by (logit desc, position asc).
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//   warp 0      issuer: 1-D bulk copies of whole 8448-byte pages into a ring of
+//               shared-memory stages (a record's 132-byte pitch is not 16-byte
+//               aligned, so tiled tensor maps cannot address rows; whole pages can).
+//   warp 1      MMA: allocates TMEM, issues tcgen05.mma kind::f8f6f4 with the
+//               128-record key tile as the A operand in TMEM and the query as the
+//               B operand in shared memory, accumulating fp32 in TMEM.
+//   warp 2      page walker: turns (query, tile) into physical pages through the
+//               page table / resident list, 32 pages at a time.
+//   warp 3      query prep: splits each bf16 query row into two e4m3 terms
+//               (q * 2^e_h = hi + lo, exact for every element of magnitude
+//               >= 2^-2 after the per-head power-of-two scale) written in the
+//               128-byte-swizzled K-major layout the MMA reads, and folds 2^-e_h
+//               into the head weight.
+//   warps 4-7   loader: copies each record's 128 e4m3 bytes from the staged page
+//               into TMEM as the A operand (raw bytes, no conversion), and its
+//               scale (NaN for an invisible record) and position beside the
+//               accumulator.
+//   warps 8-11  epilogue: reads the fp32 head dots from TMEM and computes
+//               s * sum_h relu(x_h) w'_h; then either writes sigmoid scores or
+//               keeps a thresholded candidate buffer in shared memory and writes
+//               each segment's best k to a workspace slot.
+// A second kernel merges the slots of each query into the exact, sorted top-k.
+//
+// Work split: a query row covers ceil(visible pages / 2) tiles of 128 records;
+// the tiles of all rows are laid end to end and cut into one contiguous,
+// equal-sized range per CTA. A CTA's range falls into "segments" (maximal runs
+// of one row); segment (row b, CTA c) owns workspace slot b + c, which is unique
+// because b + c grows by at least one from one segment to the next.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "csa_index.h"
+#include "csa_ptx.cuh"
+#include "csa_select.cuh"
+
+namespace csa {
+
+constexpr int kH = 64;
+constexpr int kD = 128;
+constexpr int kPage = 64;
+constexpr int kRec = 132;
+constexpr int kPageBytes = kPage * kRec;  // 8448
+constexpr int kTile = 128;                // records per MMA tile (two pages)
+
+constexpr int kStages = 12;  // page stages in shared memory
+constexpr int kAStages = 4;  // TMEM A (key tile) stages
+constexpr int kDStages = 4;  // TMEM accumulator stages
+constexpr int kRing = 4;     // page-walker ring slots of 32 pages
+constexpr int kCap = 4096;   // candidate buffer of one segment (keys)
+
+constexpr int kThreads = 384;
+constexpr int kWarpIssuer = 0, kWarpMma = 1, kWarpWalker = 2, kWarpQprep = 3, kWarpLoader = 4, kWarpEpi = 8;
+constexpr int kBarLoader = 1, kBarEpi = 2;
+
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t a_col(int s) { return static_cast<uint32_t>(s) * 32u; }
+__host__ __device__ constexpr uint32_t d_col(int s) { return 128u + static_cast<uint32_t>(s) * 64u; }
+__host__ __device__ constexpr uint32_t si_col(int s) { return 384u + static_cast<uint32_t>(s) * 2u; }
+static_assert(si_col(kDStages) <= kTmemCols, "TMEM column map");
+static_assert(a_col(kAStages) <= d_col(0), "TMEM column map");
+
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 64);
+constexpr uint32_t kNaNBits = 0x7FC00000u;
+
+struct Params {
+  const uint16_t* q;
+  const float* w;
+  const uint8_t* kv;
+  int64_t num_pages;
+  int64_t page_stride;
+  const int32_t* page_table;
+  const int32_t* q_req;
+  const int32_t* q_len;
+  const int32_t* resident;
+  const int32_t* n_resident;
+  int32_t* dev_status;
+  float* scores;        // score mode
+  const float* in_scores;  // unfused top-k
+  int64_t score_stride;
+  uint8_t* ws;          // top-k modes
+  int64_t slot_bytes;
+  int64_t slots_offset;
+  int32_t num_q;
+  int32_t num_req;
+  int32_t pt_stride;
+  int32_t res_stride;
+  int32_t k;
+  int32_t grid;         // CTAs of the phase-1 kernel (slot numbering)
+};
+
+struct PageInfo {
+  int32_t lp;     // logical page (positions lp*64 + r)
+  int32_t nrows;  // visible rows of the page (0: nothing to score)
+  int32_t phys;   // physical page
+  int32_t pad;
+};
+
+// ------------------------------------------------------------------ geometry
+
+// Request of row b, or -1 when out of range.
+__device__ __forceinline__ int32_t row_request(const Params& P, int32_t b) {
+  const int32_t req = P.q_req ? P.q_req[b] : b;
+  return (req < 0 || req >= P.num_req) ? -1 : req;
+}
+
+// Visible length of row b: q_len clamped to [0, 64 * pt_stride].
+__device__ __forceinline__ int64_t row_length(const Params& P, int32_t b, int32_t* flags) {
+  int64_t L = P.q_len[b];
+  const int64_t cap = static_cast<int64_t>(kPage) * P.pt_stride;
+  if (L < 0) {
+    *flags |= CSA_DEV_LEN_OOB;
+    L = 0;
+  }
+  if (L > cap) {
+    *flags |= CSA_DEV_LEN_OOB;
+    L = cap;
+  }
+  return L;
+}
+
+__device__ __forceinline__ int32_t resident_count(const Params& P, int32_t req, int32_t* flags) {
+  int32_t n = P.n_resident[req];
+  if (n < 0) {
+    *flags |= CSA_DEV_LEN_OOB;
+    n = 0;
+  }
+  if (n > P.res_stride) {
+    *flags |= CSA_DEV_LEN_OOB;
+    n = P.res_stride;
+  }
+  return n;
+}
+
+// Tiles of 128 records (two page slots) that row b covers.
+__device__ __forceinline__ int64_t query_tiles(const Params& P, int32_t b, int32_t* flags) {
+  const int32_t req = row_request(P, b);
+  if (req < 0) {
+    *flags |= CSA_DEV_BAD_REQUEST;
+    return 0;
+  }
+  if (P.resident) return (resident_count(P, req, flags) + 1) / 2;
+  return (row_length(P, b, flags) + kTile - 1) / kTile;
+}
+
+__device__ __forceinline__ int64_t query_tiles(const Params& P, int32_t b) {
+  int32_t f = 0;
+  return query_tiles(P, b, &f);
+}
+
+__device__ __forceinline__ int32_t next_nonempty(const Params& P, int32_t b) {
+  while (b < P.num_q && query_tiles(P, b) == 0) ++b;
+  return b;
+}
+
+__host__ __device__ __forceinline__ int64_t cta_begin(int64_t c, int64_t total, int64_t grid) {
+  return c * total / grid;
+}
+
+// CTA whose (non-empty) range holds tile t, 0 <= t < total.
+__host__ __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t total, int64_t grid) {
+  const int64_t c = ((t + 1) * grid - 1) / total;
+  return c < grid - 1 ? c : grid - 1;
+}
+
+// Visible rows, logical page and physical page of page slot `half` of tile
+// `lt` of row b. nrows = 0 marks a slot with nothing to score.
+__device__ PageInfo page_of(const Params& P, int32_t b, int64_t lt, int half, int32_t* flags) {
+  PageInfo e{0, 0, 0, 0};
+  const int32_t req = row_request(P, b);
+  if (req < 0) return e;
+  const int64_t L = row_length(P, b, flags);
+  const int64_t npages = (L + kPage - 1) / kPage;
+  const int64_t slot = 2 * lt + half;
+  int64_t p;
+  if (P.resident) {
+    if (slot >= resident_count(P, req, flags)) return e;
+    p = P.resident[static_cast<int64_t>(req) * P.res_stride + slot];
+    if (p < 0 || p >= npages) {
+      *flags |= CSA_DEV_RESIDENT_OOB;
+      return e;
+    }
+  } else {
+    p = slot;
+    if (p >= npages) return e;
+  }
+  e.lp = static_cast<int32_t>(p);
+  if (P.page_table) {  // the unfused top-k may run without a page table
+    const int32_t phys = P.page_table[static_cast<int64_t>(req) * P.pt_stride + p];
+    if (phys < 0 || phys >= P.num_pages) {
+      *flags |= CSA_DEV_PAGE_OOB;
+      return e;
+    }
+    e.phys = phys;
+  }
+  const int64_t rows = L - p * kPage;
+  e.nrows = static_cast<int32_t>(rows < kPage ? rows : kPage);
+  return e;
+}
+
+// ------------------------------------------------------------------ planning
+
+struct Plan {
+  int64_t total;   // tiles of all rows
+  int64_t t0;      // first tile of this CTA
+  int64_t ntiles;  // tiles of this CTA
+  int64_t lt0;     // local tile of row b0 at t0
+  int32_t b0;      // row holding tile t0
+  int32_t flags;
+};
+
+// Block-wide: tiles of every row, their running sum, and this CTA's share.
+// CTA 0 also writes the exclusive prefix sums (tile_off[num_q + 1]) when given.
+template <int NT>
+__device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32_t* tile_off) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = NT / 32;
+  int32_t flags = 0;
+  // pass 1: total
+  int64_t part = 0;
+  for (int32_t b = tid; b < P.num_q; b += NT) part += query_tiles(P, b, &flags);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+  if (lane == 0) warp_sums[warp] = part;
+  __syncthreads();
+  int64_t total = 0;
+  for (int i = 0; i < NW; ++i) total += warp_sums[i];
+  __syncthreads();
+  const int64_t t0 = cta_begin(blockIdx.x, total, gridDim.x);
+  const int64_t t1 = cta_begin(blockIdx.x + 1, total, gridDim.x);
+  if (tid == 0) {
+    plan->total = total;
+    plan->t0 = t0;
+    plan->ntiles = t1 - t0;
+    plan->b0 = P.num_q;
+    plan->lt0 = 0;
+  }
+  // pass 2: ordered prefix sums, chunk by chunk
+  const bool write_off = tile_off != nullptr && blockIdx.x == 0;
+  int64_t running = 0;
+  for (int32_t base = 0; base < P.num_q; base += NT) {
+    const int32_t b = base + tid;
+    const int64_t t = b < P.num_q ? query_tiles(P, b) : 0;
+    int64_t incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int64_t before = running;
+    for (int i = 0; i < warp; ++i) before += warp_sums[i];
+    int64_t chunk = 0;
+    for (int i = 0; i < NW; ++i) chunk += warp_sums[i];
+    const int64_t excl = before + incl - t;
+    if (b < P.num_q) {
+      if (write_off) tile_off[b] = static_cast<int32_t>(excl);
+      if (t > 0 && excl <= t0 && t0 < excl + t) {
+        plan->b0 = b;
+        plan->lt0 = t0 - excl;
+      }
+    }
+    running += chunk;
+    if (!write_off && running > t0) break;  // uniform: every thread sees the same running sum
+  }
+  if (write_off && tid == 0) tile_off[P.num_q] = static_cast<int32_t>(total);
+  if (flags) atomicOr(&plan->flags, flags);
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ shared memory
+
+struct __align__(1024) Smem {
+  uint8_t qbuf[2][2][kH * kD];     // [slot][hi/lo] e4m3, K-major, 128-byte swizzle
+  uint8_t pages[kStages][kPageBytes];
+  uint64_t cand[kCap];
+  uint64_t scratch[CSA_MAX_K];
+  float wbuf[2][kH];
+  PageInfo ring[kRing * 32];
+  PageInfo info[kStages];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t afull[kAStages], aempty[kAStages];
+  uint64_t dfull[kDStages], dempty[kDStages];
+  uint64_t qfull[2], qempty[2];
+  uint64_t rfull[kRing], rempty[kRing];
+  uint64_t drain;
+  SelectShared sel;
+  Plan plan;
+  int64_t warp_sums[32];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t status;
+  int32_t go[2][2];                // [group][iteration parity] broadcast of a leader's wait result
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ Smem& smem_of(uint8_t* raw) {
+  return *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
+// ------------------------------------------------------------------ roles
+
+struct Cursor {
+  int32_t b;
+  int64_t lt;
+  int64_t tiles;
+  __device__ void init(const Params& P, const Plan& pl) {
+    b = pl.b0;
+    lt = pl.lt0;
+    tiles = b < P.num_q ? query_tiles(P, b) : 0;
+  }
+  __device__ void advance(const Params& P) {
+    if (++lt >= tiles) {
+      b = next_nonempty(P, b + 1);
+      lt = 0;
+      tiles = b < P.num_q ? query_tiles(P, b) : 0;
+    }
+  }
+};
+
+__device__ void role_walker(const Params& P, Smem& S) {
+  const int lane = threadIdx.x & 31;
+  const int64_t npg = 2 * S.plan.ntiles;
+  Cursor cur;
+  cur.init(P, S.plan);
+  int32_t flags = 0;
+  for (int64_t pg = 0; pg < npg; pg += 32) {
+    const int64_t batch = pg >> 5;
+    const int slot = static_cast<int>(batch % kRing);
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_u32(&S.rempty[slot]), static_cast<uint32_t>(((batch / kRing) & 1) ^ 1),
+                                  &S.abort_flag);
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+    // lane j handles page pg + j: tile offset j / 2, slot j % 2
+    int32_t bb = cur.b;
+    int64_t ll = cur.lt + (lane >> 1), tb = cur.tiles;
+    while (bb < P.num_q && ll >= tb) {
+      ll -= tb;
+      bb = next_nonempty(P, bb + 1);
+      tb = bb < P.num_q ? query_tiles(P, bb) : 0;
+    }
+    PageInfo e{0, -1, 0, 0};
+    if (pg + lane < npg && bb < P.num_q) e = page_of(P, bb, ll, lane & 1, &flags);
+    S.ring[slot * 32 + lane] = e;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.rfull[slot]));
+    // the cursor moves on by 16 tiles
+    for (int t = 0; t < 16; ++t) cur.advance(P);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
+  if (lane == 0 && flags) atomicOr(&S.status, flags);
+}
+
+__device__ void role_issuer(const Params& P, Smem& S) {
+  const int64_t npg = 2 * S.plan.ntiles;
+  const uint64_t policy = policy_evict_first();
+  int64_t pg = 0;
+  for (; pg < npg; ++pg) {
+    const int64_t batch = pg >> 5;
+    const int slot = static_cast<int>(batch % kRing);
+    const int j = static_cast<int>(pg & 31);
+    if (j == 0 && !mbar_wait(smem_u32(&S.rfull[slot]), static_cast<uint32_t>((batch / kRing) & 1), &S.abort_flag))
+      break;
+    const PageInfo e = S.ring[slot * 32 + j];
+    const int s = static_cast<int>(pg % kStages);
+    if (!mbar_wait(smem_u32(&S.empty[s]), static_cast<uint32_t>(((pg / kStages) & 1) ^ 1), &S.abort_flag)) break;
+    S.info[s] = e;
+    const uint32_t fb = smem_u32(&S.full[s]);
+    if (e.nrows > 0) {
+      mbar_arrive_expect_tx(fb, kPageBytes);
+      bulk_g2s_hint(smem_u32(S.pages[s]), P.kv + static_cast<int64_t>(e.phys) * P.page_stride, kPageBytes, fb,
+                    policy);
+    } else {
+      mbar_arrive(fb);
+    }
+    if (j == 31 || pg == npg - 1) mbar_arrive(smem_u32(&S.rempty[slot]));
+  }
+  // Wait for every copy still in flight before the CTA may exit.
+  for (int64_t p = pg - 1; p >= 0 && p >= pg - kStages; --p)
+    mbar_wait_drain(smem_u32(&S.full[p % kStages]), static_cast<uint32_t>((p / kStages) & 1));
+}
+
+__device__ void role_mma(const Params& P, Smem& S) {
+  Cursor cur;
+  cur.init(P, S.plan);
+  const uint32_t tmem = S.tmem_base;
+  int seg = 0;
+  for (int64_t i = 0; i < S.plan.ntiles; ++i) {
+    const bool seg_start = (i == 0) || (cur.lt == 0);
+    if (seg_start && i > 0) ++seg;
+    const int qs = seg & 1;
+    const int ta = static_cast<int>(i % kAStages), td = static_cast<int>(i % kDStages);
+    if (seg_start &&
+        !mbar_wait(smem_u32(&S.qfull[qs]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag))
+      break;
+    if (!mbar_wait(smem_u32(&S.afull[ta]), static_cast<uint32_t>((i / kAStages) & 1), &S.abort_flag)) break;
+    if (!mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((i / kDStages) & 1) ^ 1), &S.abort_flag))
+      break;
+    tc_fence_after();
+    const uint32_t dt = tmem + d_col(td);
+    const uint32_t at = tmem + a_col(ta);
+#pragma unroll
+    for (int term = 0; term < 2; ++term) {
+      const uint32_t bq = smem_u32(S.qbuf[qs][term]);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc, (term | kk) != 0);
+      }
+    }
+    mma_commit(smem_u32(&S.aempty[ta]));
+    mma_commit(smem_u32(&S.dfull[td]));
+    const bool seg_end = (i == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
+    if (seg_end) mma_commit(smem_u32(&S.qempty[qs]));
+    cur.advance(P);
+  }
+  mma_commit(smem_u32(&S.drain));
+  mbar_wait_drain(smem_u32(&S.drain), 0);
+}
+
+// Splits one bf16 query row into e4m3 hi + lo terms (per-head power-of-two
+// scale so that the largest |q| maps into (224, 448]) in the swizzled layout.
+__device__ void prep_query(const Params& P, Smem& S, int32_t b, int qs, int32_t* flags) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t* qrow = P.q + static_cast<int64_t>(b) * kH * kD;
+  uint8_t* hi = S.qbuf[qs][0];
+  uint8_t* lo = S.qbuf[qs][1];
+  for (int h0 = 0; h0 < kH; h0 += 8) {
+    uint2 raw[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) raw[j] = *reinterpret_cast<const uint2*>(qrow + (h0 + j) * kD + lane * 4);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int h = h0 + j;
+      float x[4];
+      x[0] = __uint_as_float(raw[j].x << 16);
+      x[1] = __uint_as_float(raw[j].x & 0xFFFF0000u);
+      x[2] = __uint_as_float(raw[j].y << 16);
+      x[3] = __uint_as_float(raw[j].y & 0xFFFF0000u);
+      float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      if (!isfinite(m)) {
+        *flags |= CSA_DEV_RANGE;
+        m = 1.0f;
+      }
+      int E2;
+      const float f = frexpf(m, &E2);
+      int e = (f <= 0.875f) ? 9 - E2 : 8 - E2;
+      e = e < -126 ? -126 : (e > 126 ? 126 : e);
+      const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+      const float isc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      uint32_t whi = 0, wlo = 0;
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const float a = x[2 * pr] * sc, c = x[2 * pr + 1] * sc;
+        uint16_t h2, l2;
+        uint32_t hf;
+        // pack: the second operand lands in the low byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h2) : "f"(c), "f"(a));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hf) : "h"(h2));
+        const float ah = __half2float(__ushort_as_half(static_cast<uint16_t>(hf & 0xFFFFu)));
+        const float ch = __half2float(__ushort_as_half(static_cast<uint16_t>(hf >> 16)));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(l2) : "f"(c - ch), "f"(a - ah));
+        whi |= static_cast<uint32_t>(h2) << (16 * pr);
+        wlo |= static_cast<uint32_t>(l2) << (16 * pr);
+      }
+      const uint32_t off = (h >> 3) * 1024 + (h & 7) * 128 + ((((lane >> 2) ^ (h & 7)) & 7) << 4) + (lane & 3) * 4;
+      *reinterpret_cast<uint32_t*>(hi + off) = whi;
+      *reinterpret_cast<uint32_t*>(lo + off) = wlo;
+      if (lane == 0) S.wbuf[qs][h] = P.w[static_cast<int64_t>(b) * kH + h] * isc;
+    }
+  }
+}
+
+__device__ void role_qprep(const Params& P, Smem& S) {
+  const int lane = threadIdx.x & 31;
+  int32_t flags = 0;
+  int32_t b = S.plan.b0;
+  int64_t done = 0;
+  int64_t first = S.plan.lt0;
+  for (int seg = 0; done < S.plan.ntiles; ++seg) {
+    const int qs = seg & 1;
+    int ok = 1;
+    if (lane == 0)
+      ok = mbar_wait(smem_u32(&S.qempty[qs]), static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), &S.abort_flag);
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+    prep_query(P, S, b, qs, &flags);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.qfull[qs]));
+    const int64_t t = query_tiles(P, b) - first;
+    done += t;
+    first = 0;
+    b = next_nonempty(P, b + 1);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
+  if (lane == 0 && flags) atomicOr(&S.status, flags);
+}
+
+__device__ void role_loader(const Params& P, Smem& S) {
+  const int g = threadIdx.x - kWarpLoader * 32;  // 0..127
+  const int q = g >> 5, lane = g & 31;
+  const int half = q >> 1;
+  const int r = g & 63;
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tmem = S.tmem_base;
+  for (int64_t i = 0; i < S.plan.ntiles; ++i) {
+    const int ta = static_cast<int>(i % kAStages), td = static_cast<int>(i % kDStages);
+    const int64_t pg0 = 2 * i;
+    const int s0 = static_cast<int>(pg0 % kStages), s1 = static_cast<int>((pg0 + 1) % kStages);
+    const uint32_t ph0 = static_cast<uint32_t>((pg0 / kStages) & 1), ph1 = static_cast<uint32_t>(((pg0 + 1) / kStages) & 1);
+    if (g == 0) {
+      const bool ok =
+          mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag) &&
+          mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((i / kDStages) & 1) ^ 1), &S.abort_flag) &&
+          mbar_wait(smem_u32(&S.full[s0]), ph0, &S.abort_flag) && mbar_wait(smem_u32(&S.full[s1]), ph1, &S.abort_flag);
+      S.go[0][i & 1] = ok ? 1 : 0;
+    }
+    named_bar_sync(kBarLoader, 128);
+    if (!S.go[0][i & 1]) break;
+    const int s = half ? s1 : s0;
+    mbar_wait_drain(smem_u32(&S.full[s]), half ? ph1 : ph0);  // already complete: acquire for this thread
+    const PageInfo e = S.info[s];
+    const uint8_t* src = S.pages[s] + r * kRec;
+    uint32_t v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = *reinterpret_cast<const uint32_t*>(src + 4 * j);
+    const uint32_t sc = *reinterpret_cast<const uint32_t*>(src + kD);
+    const bool valid = r < e.nrows;
+    tmem_st32(tmem + a_col(ta) + lane_off, v);
+    tmem_st2(tmem + si_col(td) + lane_off, valid ? sc : kNaNBits,
+             static_cast<uint32_t>(e.lp * kPage + r));
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&S.empty[s]));
+      mbar_arrive(smem_u32(&S.afull[ta]));
+    }
+  }
+}
+
+template <bool kTopk>
+__device__ void role_epilogue(const Params& P, Smem& S) {
+  const int g = threadIdx.x - kWarpEpi * 32;  // 0..127
+  const int q = g >> 5, lane = g & 31;
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tmem = S.tmem_base;
+  Cursor cur;
+  cur.init(P, S.plan);
+  int seg = 0;
+  float w[kH];
+  for (int64_t i = 0; i < S.plan.ntiles; ++i) {
+    const bool seg_start = (i == 0) || (cur.lt == 0);
+    if (seg_start && i > 0) ++seg;
+    const int qs = seg & 1;
+    const int td = static_cast<int>(i % kDStages);
+    const uint32_t qph = static_cast<uint32_t>((seg >> 1) & 1);
+    const uint32_t dph = static_cast<uint32_t>((i / kDStages) & 1);
+    if (g == 0) {
+      const bool ok = (!seg_start || mbar_wait(smem_u32(&S.qfull[qs]), qph, &S.abort_flag)) &&
+                      mbar_wait(smem_u32(&S.dfull[td]), dph, &S.abort_flag);
+      S.go[1][i & 1] = ok ? 1 : 0;
+    }
+    named_bar_sync(kBarEpi, 128);
+    if (!S.go[1][i & 1]) break;
+    if (seg_start) {
+      mbar_wait_drain(smem_u32(&S.qfull[qs]), qph);
+#pragma unroll
+      for (int h = 0; h < kH; ++h) w[h] = S.wbuf[qs][h];
+    }
+    mbar_wait_drain(smem_u32(&S.dfull[td]), dph);
+    tc_fence_after();
+    uint32_t x0[32], x1[32];
+    uint32_t sc_bits, pos_bits;
+    tmem_ld32(tmem + d_col(td) + lane_off, x0);
+    tmem_ld32(tmem + d_col(td) + 32 + lane_off, x1);
+    tmem_ld2(tmem + si_col(td) + lane_off, sc_bits, pos_bits);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
+
+    const float s = __uint_as_float(sc_bits);
+    const bool valid = !isnan(s);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (s >= 0.0f) {
+#pragma unroll
+      for (int h = 0; h < 32; h += 4) {
+        a0 = fmaf(fmaxf(__uint_as_float(x0[h]), 0.f), w[h], a0);
+        a1 = fmaf(fmaxf(__uint_as_float(x0[h + 1]), 0.f), w[h + 1], a1);
+        a2 = fmaf(fmaxf(__uint_as_float(x0[h + 2]), 0.f), w[h + 2], a2);
+        a3 = fmaf(fmaxf(__uint_as_float(x0[h + 3]), 0.f), w[h + 3], a3);
+      }
+#pragma unroll
+      for (int h = 0; h < 32; h += 4) {
+        a0 = fmaf(fmaxf(__uint_as_float(x1[h]), 0.f), w[32 + h], a0);
+        a1 = fmaf(fmaxf(__uint_as_float(x1[h + 1]), 0.f), w[32 + h + 1], a1);
+        a2 = fmaf(fmaxf(__uint_as_float(x1[h + 2]), 0.f), w[32 + h + 2], a2);
+        a3 = fmaf(fmaxf(__uint_as_float(x1[h + 3]), 0.f), w[32 + h + 3], a3);
+      }
+    } else {
+      // relu(s * x) = s * min(x, 0) for s < 0
+#pragma unroll
+      for (int h = 0; h < 32; h += 4) {
+        a0 = fmaf(fminf(__uint_as_float(x0[h]), 0.f), w[h], a0);
+        a1 = fmaf(fminf(__uint_as_float(x0[h + 1]), 0.f), w[h + 1], a1);
+        a2 = fmaf(fminf(__uint_as_float(x0[h + 2]), 0.f), w[h + 2], a2);
+        a3 = fmaf(fminf(__uint_as_float(x0[h + 3]), 0.f), w[h + 3], a3);
+      }
+#pragma unroll
+      for (int h = 0; h < 32; h += 4) {
+        a0 = fmaf(fminf(__uint_as_float(x1[h]), 0.f), w[32 + h], a0);
+        a1 = fmaf(fminf(__uint_as_float(x1[h + 1]), 0.f), w[32 + h + 1], a1);
+        a2 = fmaf(fminf(__uint_as_float(x1[h + 2]), 0.f), w[32 + h + 2], a2);
+        a3 = fmaf(fminf(__uint_as_float(x1[h + 3]), 0.f), w[32 + h + 3], a3);
+      }
+    }
+    const float logit = s * ((a0 + a1) + (a2 + a3));
+    const int32_t pos = static_cast<int32_t>(pos_bits);
+
+    if constexpr (!kTopk) {
+      if (valid) {
+        const int64_t col = cur.lt * kTile + g;
+        P.scores[static_cast<int64_t>(cur.b) * P.score_stride + col] = 1.0f / (1.0f + expf(-logit));
+      }
+    } else {
+      const uint64_t key = (valid && !isnan(logit)) ? make_key(logit, pos) : 0ull;
+      append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+      named_bar_sync(kBarEpi, 128);
+      shrink_if_above<128>(S.cand, S.scratch, kCap - 128, P.k, &S.sel, kBarEpi, g);
+    }
+
+    const bool seg_end = (i == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
+    if (seg_end) {
+      if constexpr (kTopk) {
+        shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, &S.sel, kBarEpi, g);
+        const int n = static_cast<int>(S.sel.n);
+        uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
+        uint64_t* ent = reinterpret_cast<uint64_t*>(slot + 16);
+        for (int j = g; j < n; j += 128) ent[j] = S.cand[j];
+        named_bar_sync(kBarEpi, 128);
+        if (g == 0) {
+          *reinterpret_cast<int32_t*>(slot) = n;
+          S.sel.n = 0;
+          S.sel.tau = 0;
+        }
+        named_bar_sync(kBarEpi, 128);
+      }
+      if (g == 0) mbar_arrive(smem_u32(&S.qempty[qs]));
+    }
+    cur.advance(P);
+  }
+}
+
+template <bool kTopk>
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = smem_of(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    S.plan.flags = 0;
+    S.abort_flag = 0;
+    S.status = 0;
+    S.sel.n = 0;
+    S.sel.tau = 0;
+  }
+  __syncthreads();
+  make_plan<kThreads>(P, &S.plan, S.warp_sums,
+                      kTopk ? reinterpret_cast<int32_t*>(P.ws) : nullptr);
+  if (tid == 0 && blockIdx.x == 0 && S.plan.flags && P.dev_status) atomicOr(P.dev_status, S.plan.flags);
+  if (S.plan.ntiles == 0) return;  // uniform
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&S.full[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), 2);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(smem_u32(&S.afull[s]), 4);
+      mbar_init(smem_u32(&S.aempty[s]), 1);
+    }
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(smem_u32(&S.dfull[s]), 1);
+      mbar_init(smem_u32(&S.dempty[s]), 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&S.qfull[s]), 1);
+      mbar_init(smem_u32(&S.qempty[s]), 2);
+    }
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_u32(&S.rfull[s]), 1);
+      mbar_init(smem_u32(&S.rempty[s]), 1);
+    }
+    mbar_init(smem_u32(&S.drain), 1);
+    mbar_init_fence();
+    fence_proxy_async_smem();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == kWarpIssuer) {
+    if ((tid & 31) == 0) role_issuer(P, S);
+  } else if (warp == kWarpMma) {
+    if ((tid & 31) == 0) role_mma(P, S);
+  } else if (warp == kWarpWalker) {
+    role_walker(P, S);
+  } else if (warp == kWarpQprep) {
+    role_qprep(P, S);
+  } else if (warp < kWarpEpi) {
+    role_loader(P, S);
+  } else {
+    role_epilogue<kTopk>(P, S);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(S.tmem_base, kTmemCols);
+  }
+  if (tid == 0 && P.dev_status) {
+    const int32_t st = S.status | (S.abort_flag ? CSA_DEV_TIMEOUT : 0);
+    if (st) atomicOr(P.dev_status, st);
+  }
+}
+
+// ------------------------------------------------------------------ merge
+
+constexpr int kMergeThreads = 256;
+constexpr int kMergeCap = 8192;
+
+struct MergeSmem {
+  uint64_t cand[kMergeCap];
+  uint64_t scratch[CSA_MAX_K];
+  SelectShared sel;
+};
+
+// One CTA per query row: gathers the row's segment slots, keeps the exact top
+// k and writes them sorted by (value desc, position asc), padded with -1 / 0.
+template <bool kFromLogit>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, int32_t* idx, float* vals) {
+  extern __shared__ uint8_t smem_raw[];
+  MergeSmem& S = *reinterpret_cast<MergeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x;
+  const int32_t b = blockIdx.x;
+  const int32_t* tile_off = reinterpret_cast<const int32_t*>(P.ws);
+  if (tid == 0) {
+    S.sel.n = 0;
+    S.sel.tau = 0;
+  }
+  __syncthreads();
+  const int64_t t0 = tile_off[b], t1 = tile_off[b + 1], total = tile_off[P.num_q];
+  if (t0 < t1) {
+    const int64_t c0 = cta_of(t0, total, P.grid), c1 = cta_of(t1 - 1, total, P.grid);
+    for (int64_t c = c0; c <= c1; ++c) {
+      if (cta_begin(c, total, P.grid) == cta_begin(c + 1, total, P.grid)) continue;
+      const uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(b) + c) * P.slot_bytes;
+      int cnt = *reinterpret_cast<const int32_t*>(slot);
+      cnt = cnt < 0 ? 0 : (cnt > P.k ? P.k : cnt);  // a slot never holds more than k keys
+      const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot + 16);
+      for (int base = 0; base < cnt; base += kMergeThreads) {
+        const uint64_t key = (base + tid < cnt) ? ent[base + tid] : 0ull;
+        append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+        __syncthreads();
+        shrink_if_above<kMergeThreads>(S.cand, S.scratch, kMergeCap - kMergeThreads, P.k, &S.sel, 0, tid);
+      }
+    }
+  }
+  shrink_if_above<kMergeThreads>(S.cand, S.scratch, P.k, P.k, &S.sel, 0, tid);
+  const int n = static_cast<int>(S.sel.n);
+  int m = 1;
+  while (m < n) m <<= 1;
+  for (int j = n + tid; j < m; j += kMergeThreads) S.cand[j] = 0ull;
+  __syncthreads();
+  if (m > 1) bitonic_sort_desc<kMergeThreads>(S.cand, m, 0, tid);
+  for (int j = tid; j < P.k; j += kMergeThreads) {
+    const int64_t o = static_cast<int64_t>(b) * P.k + j;
+    if (j < n) {
+      const uint64_t key = S.cand[j];
+      const float v = key_value(key);
+      idx[o] = key_position(key);
+      vals[o] = kFromLogit ? 1.0f / (1.0f + expf(-v)) : v;
+    } else {
+      idx[o] = -1;
+      vals[o] = 0.0f;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ unfused top-k
+
+constexpr int kTopkThreads = 128;
+constexpr int kTopkBatch = 8;
+constexpr int kTopkCtasPerSm = 4;
+
+struct TopkSmem {
+  uint64_t cand[kCap];
+  uint64_t scratch[CSA_MAX_K];
+  SelectShared sel;
+  Plan plan;
+  int64_t warp_sums[32];
+};
+
+// Phase 1 of top-k over a score matrix: same tiles, CTA ranges and slots as the
+// fused kernel; each thread owns one column of a 128-column tile.
+__global__ void __launch_bounds__(kTopkThreads) topk_scores_kernel(const Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkSmem& S = *reinterpret_cast<TopkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    S.plan.flags = 0;
+    S.sel.n = 0;
+    S.sel.tau = 0;
+  }
+  __syncthreads();
+  make_plan<kTopkThreads>(P, &S.plan, S.warp_sums, reinterpret_cast<int32_t*>(P.ws));
+  if (tid == 0 && blockIdx.x == 0 && S.plan.flags && P.dev_status) atomicOr(P.dev_status, S.plan.flags);
+  if (S.plan.ntiles == 0) return;
+  int32_t flags = 0;
+  Cursor cur;
+  cur.init(P, S.plan);
+  for (int64_t i0 = 0; i0 < S.plan.ntiles; i0 += kTopkBatch) {
+    const int nb = static_cast<int>(S.plan.ntiles - i0 < kTopkBatch ? S.plan.ntiles - i0 : kTopkBatch);
+    float val[kTopkBatch];
+    int32_t pos[kTopkBatch];
+    bool ok[kTopkBatch];
+    Cursor c = cur;
+#pragma unroll
+    for (int u = 0; u < kTopkBatch; ++u) {
+      ok[u] = false;
+      pos[u] = 0;
+      val[u] = 0.f;
+      if (u < nb) {
+        const int64_t col = c.lt * kTile + tid;
+        const PageInfo e = page_of(P, c.b, c.lt, tid >> 6, &flags);
+        const int r = tid & 63;
+        if (r < e.nrows) {
+          ok[u] = true;
+          pos[u] = e.lp * kPage + r;
+          val[u] = P.in_scores[static_cast<int64_t>(c.b) * P.score_stride + col];
+        }
+        c.advance(P);
+      }
+    }
+    for (int u = 0; u < nb; ++u) {
+      const uint64_t key = (ok[u] && !isnan(val[u])) ? make_key(val[u], pos[u]) : 0ull;
+      append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+      __syncthreads();
+      shrink_if_above<kTopkThreads>(S.cand, S.scratch, kCap - kTopkThreads, P.k, &S.sel, 0, tid);
+      const bool seg_end = (i0 + u == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
+      if (seg_end) {
+        shrink_if_above<kTopkThreads>(S.cand, S.scratch, P.k, P.k, &S.sel, 0, tid);
+        const int n = static_cast<int>(S.sel.n);
+        uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
+        uint64_t* ent = reinterpret_cast<uint64_t*>(slot + 16);
+        for (int j = tid; j < n; j += kTopkThreads) ent[j] = S.cand[j];
+        __syncthreads();
+        if (tid == 0) {
+          *reinterpret_cast<int32_t*>(slot) = n;
+          S.sel.n = 0;
+          S.sel.tau = 0;
+        }
+        __syncthreads();
+      }
+      cur.advance(P);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
+  if ((tid & 31) == 0 && flags && P.dev_status) atomicOr(P.dev_status, flags);
+}
+
+}  // namespace csa
+
+// ====================================================================== C ABI
+
+namespace {
+
+using namespace csa;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+bool g_ready[kMaxDevices];
+
+size_t slot_bytes_for(int32_t k) { return (16 + 8 * static_cast<size_t>(k) + 15) & ~size_t(15); }
+size_t slots_offset_for(int32_t num_q) { return (4 * (static_cast<size_t>(num_q) + 1) + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+enum { kNeedQ = 1, kNeedKv = 2 };
+
+csa_status check_args(const csa_index_args* a, int need) {
+  if (!a) return CSA_ERR_INVALID_ARG;
+  if (a->reserved0 != 0 || a->reserved1 != 0) return CSA_ERR_INVALID_ARG;
+  if (a->num_q < 0 || a->num_req < 0 || a->pt_stride < 0 || a->res_stride < 0) return CSA_ERR_INVALID_ARG;
+  if (a->num_q == 0) return CSA_OK;
+  if (!a->q_len) return CSA_ERR_INVALID_ARG;
+  if (!aligned(a->q_len, 4) || (a->q_req && !aligned(a->q_req, 4))) return CSA_ERR_ALIGNMENT;
+  if (!a->q_req && a->num_req < a->num_q) return CSA_ERR_INVALID_ARG;
+  if (a->resident) {
+    if (!a->n_resident || a->res_stride < 1) return CSA_ERR_INVALID_ARG;
+    if (!aligned(a->resident, 4) || !aligned(a->n_resident, 4)) return CSA_ERR_ALIGNMENT;
+  }
+  if (a->dev_status && !aligned(a->dev_status, 4)) return CSA_ERR_ALIGNMENT;
+  if (need & kNeedQ) {
+    if (a->num_heads != kH || a->head_dim != kD) return CSA_ERR_UNSUPPORTED;
+    if (!a->q || !a->fused_w) return CSA_ERR_INVALID_ARG;
+    if (!aligned(a->q, 16) || !aligned(a->fused_w, 4)) return CSA_ERR_ALIGNMENT;
+  }
+  if (need & kNeedKv) {
+    if (!a->kv || !a->page_table || a->num_pages < 1 || a->pt_stride < 1 || a->num_req < 1)
+      return CSA_ERR_INVALID_ARG;
+    if (a->num_pages > INT32_MAX) return CSA_ERR_INVALID_ARG;
+    if (a->page_stride_bytes < kPageBytes) return CSA_ERR_INVALID_ARG;
+    if (a->page_stride_bytes % 16 != 0 || !aligned(a->kv, 16)) return CSA_ERR_ALIGNMENT;
+    if (!aligned(a->page_table, 4)) return CSA_ERR_ALIGNMENT;
+  } else if (a->page_table && !aligned(a->page_table, 4)) {
+    return CSA_ERR_ALIGNMENT;
+  }
+  if (static_cast<int64_t>(kPage) * a->pt_stride > INT32_MAX) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+csa_status device_setup(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ready[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return CSA_ERR_CUDA;
+    if (n * kTopkCtasPerSm > CSA_MAX_CTAS) return CSA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(MergeSmem) + 16)) != cudaSuccess ||
+        cudaFuncSetAttribute(merge_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(MergeSmem) + 16)) != cudaSuccess ||
+        cudaFuncSetAttribute(topk_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(TopkSmem) + 16)) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    g_sms[dev] = n;
+    g_ready[dev] = true;
+  }
+  *sms = g_sms[dev];
+  return CSA_OK;
+}
+
+Params params_of(const csa_index_args* a) {
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  P.q = static_cast<const uint16_t*>(a->q);
+  P.w = a->fused_w;
+  P.kv = a->kv;
+  P.num_pages = a->num_pages;
+  P.page_stride = a->page_stride_bytes;
+  P.page_table = a->page_table;
+  P.q_req = a->q_req;
+  P.q_len = a->q_len;
+  P.resident = a->resident;
+  P.n_resident = a->n_resident;
+  P.dev_status = a->dev_status;
+  P.num_q = a->num_q;
+  P.num_req = a->num_req;
+  P.pt_stride = a->pt_stride;
+  P.res_stride = a->res_stride;
+  return P;
+}
+
+int64_t min_score_stride(const csa_index_args* a) {
+  return static_cast<int64_t>(kPage) * (a->resident ? a->res_stride : a->pt_stride);
+}
+
+csa_status launch_status() { return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa_index_abi_version(void) { return CSA_ABI_VERSION; }
+
+const char* csa_status_str(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case CSA_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+size_t csa_index_workspace_bytes(const csa_index_args* args, int32_t k) {
+  if (!args || args->num_q < 0 || k < 1 || k > CSA_MAX_K) return 0;
+  return slots_offset_for(args->num_q) +
+         (static_cast<size_t>(args->num_q) + CSA_MAX_CTAS) * slot_bytes_for(k);
+}
+
+csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t score_stride, void* stream) {
+  csa_status st = check_args(args, kNeedQ | kNeedKv);
+  if (st != CSA_OK) return st;
+  if (args->num_q == 0) return CSA_OK;
+  if (!scores) return CSA_ERR_INVALID_ARG;
+  if (!aligned(scores, 4)) return CSA_ERR_ALIGNMENT;
+  if (score_stride < min_score_stride(args)) return CSA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != CSA_OK) return st;
+  Params P = params_of(args);
+  P.scores = scores;
+  P.score_stride = score_stride;
+  P.grid = sms;
+  score_kernel<false><<<sms, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(P);
+  return launch_status();
+}
+
+csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int32_t* idx, float* vals, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  csa_status st = check_args(args, kNeedQ | kNeedKv);
+  if (st != CSA_OK) return st;
+  if (k < 1 || k > CSA_MAX_K) return CSA_ERR_INVALID_ARG;
+  if (args->num_q == 0) return CSA_OK;
+  if (!idx || !vals) return CSA_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || !aligned(vals, 4)) return CSA_ERR_ALIGNMENT;
+  if (!ws || ws_bytes < csa_index_workspace_bytes(args, k)) return CSA_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return CSA_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != CSA_OK) return st;
+  Params P = params_of(args);
+  P.ws = static_cast<uint8_t*>(ws);
+  P.k = k;
+  P.slot_bytes = static_cast<int64_t>(slot_bytes_for(k));
+  P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
+  P.grid = sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  score_kernel<true><<<sms, kThreads, kSmemBytes, s>>>(P);
+  if ((st = launch_status()) != CSA_OK) return st;
+  merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
+  return launch_status();
+}
+
+csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_index_args* args, int32_t k,
+                          int32_t* idx, float* vals, void* ws, size_t ws_bytes, void* stream) {
+  csa_status st = check_args(args, 0);
+  if (st != CSA_OK) return st;
+  if (k < 1 || k > CSA_MAX_K) return CSA_ERR_INVALID_ARG;
+  if (args->num_q == 0) return CSA_OK;
+  if (args->pt_stride < 1 || args->num_req < 1) return CSA_ERR_INVALID_ARG;
+  if (!scores || !idx || !vals) return CSA_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(idx, 4) || !aligned(vals, 4)) return CSA_ERR_ALIGNMENT;
+  if (score_stride < min_score_stride(args)) return CSA_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < csa_index_workspace_bytes(args, k)) return CSA_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return CSA_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != CSA_OK) return st;
+  Params P = params_of(args);
+  P.num_pages = args->page_table ? args->num_pages : 0;
+  P.in_scores = scores;
+  P.score_stride = score_stride;
+  P.ws = static_cast<uint8_t*>(ws);
+  P.k = k;
+  P.slot_bytes = static_cast<int64_t>(slot_bytes_for(k));
+  P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
+  P.grid = sms * kTopkCtasPerSm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  topk_scores_kernel<<<P.grid, kTopkThreads, sizeof(TopkSmem) + 16, s>>>(P);
+  if ((st = launch_status()) != CSA_OK) return st;
+  merge_kernel<false><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
+  return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,236 @@
+"""Thin Python binding of libcsa_index.so (include/csa_index.h).
+
+Argument marshalling only: every step of the indexer runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. The library
+must have been built (`sparse_attention_kv_e4m3_gb300.build.build()`); there is
+no fallback, and calling without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+CSA_OK = 0
+STATUS_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_ALIGNMENT",
+                4: "CSA_ERR_WORKSPACE", 5: "CSA_ERR_CUDA"}
+DEV_PAGE_OOB, DEV_RESIDENT_OOB, DEV_RANGE, DEV_TIMEOUT, DEV_BAD_REQUEST, DEV_LEN_OOB = 1, 2, 4, 8, 16, 32
+HEAD_DIM, NUM_HEADS, RECORD_BYTES, PAGE_RECORDS, PAGE_BYTES, MAX_K, MAX_CTAS = 128, 64, 132, 64, 8448, 1024, 1024
+
+
+class CsaError(RuntimeError):
+    def __init__(self, what: str, status: int, text: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({text})")
+        self.status = status
+
+
+class Args(ctypes.Structure):
+    """Mirror of `csa_index_args`."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("fused_w", ctypes.c_void_p),
+        ("num_q", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("kv", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int64),
+        ("page_stride_bytes", ctypes.c_int64),
+        ("page_table", ctypes.c_void_p),
+        ("num_req", ctypes.c_int32),
+        ("pt_stride", ctypes.c_int32),
+        ("q_req", ctypes.c_void_p),
+        ("q_len", ctypes.c_void_p),
+        ("resident", ctypes.c_void_p),
+        ("n_resident", ctypes.c_void_p),
+        ("res_stride", ctypes.c_int32),
+        ("reserved1", ctypes.c_int32),
+        ("dev_status", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Loads the library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build it with sparse_attention_kv_e4m3_gb300.build.build()")
+            lib = ctypes.CDLL(p)
+            A = ctypes.POINTER(Args)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            lib.csa_index_abi_version.argtypes = []
+            lib.csa_index_abi_version.restype = i32
+            lib.csa_status_str.argtypes = [ctypes.c_int]
+            lib.csa_status_str.restype = ctypes.c_char_p
+            lib.csa_index_workspace_bytes.argtypes = [A, i32]
+            lib.csa_index_workspace_bytes.restype = sz
+            lib.csa_index_score.argtypes = [A, vp, i64, vp]
+            lib.csa_index_score.restype = ctypes.c_int
+            lib.csa_index_topk.argtypes = [vp, i64, A, i32, vp, vp, vp, sz, vp]
+            lib.csa_index_topk.restype = ctypes.c_int
+            lib.csa_index_score_topk_fused.argtypes = [A, i32, vp, vp, vp, sz, vp]
+            lib.csa_index_score_topk_fused.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return load().csa_status_str(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(st: int, what: str):
+    if st != CSA_OK:
+        raise CsaError(what, st, status_str(st))
+
+
+@dataclass
+class Problem:
+    """Device tensors of one indexer call (the fields of `csa_index_args`).
+
+    q [num_q, 64, 128] bf16; fused_w [num_q, 64] fp32; kv [num_pages, page_stride]
+    uint8; page_table [num_req, pt_stride] int32; q_len [num_q] int32; optional
+    q_req [num_q], resident [num_req, res_stride], n_resident [num_req] int32 and
+    dev_status [1] int32.
+    """
+
+    q: Optional[torch.Tensor]
+    fused_w: Optional[torch.Tensor]
+    kv: Optional[torch.Tensor]
+    page_table: Optional[torch.Tensor]
+    q_len: torch.Tensor
+    q_req: Optional[torch.Tensor] = None
+    resident: Optional[torch.Tensor] = None
+    n_resident: Optional[torch.Tensor] = None
+    dev_status: Optional[torch.Tensor] = None
+    num_req: Optional[int] = None
+
+    def args(self) -> Args:
+        a = Args()
+        nq = int(self.q_len.shape[0])
+        a.q = _ptr(self.q)
+        a.fused_w = _ptr(self.fused_w)
+        a.num_q = nq
+        a.num_heads = int(self.q.shape[1]) if self.q is not None else NUM_HEADS
+        a.head_dim = int(self.q.shape[2]) if self.q is not None else HEAD_DIM
+        a.kv = _ptr(self.kv)
+        if self.kv is not None:
+            a.num_pages = int(self.kv.shape[0])
+            a.page_stride_bytes = int(self.kv.stride(0)) * self.kv.element_size()
+        a.page_table = _ptr(self.page_table)
+        if self.page_table is not None:
+            a.num_req = int(self.page_table.shape[0])
+            a.pt_stride = int(self.page_table.stride(0))
+        if self.num_req is not None:
+            a.num_req = int(self.num_req)
+        a.q_req = _ptr(self.q_req)
+        a.q_len = _ptr(self.q_len)
+        a.resident = _ptr(self.resident)
+        a.n_resident = _ptr(self.n_resident)
+        if self.resident is not None:
+            a.res_stride = int(self.resident.stride(0))
+        a.dev_status = _ptr(self.dev_status)
+        return a
+
+    @property
+    def num_q(self) -> int:
+        return int(self.q_len.shape[0])
+
+    def score_stride(self) -> int:
+        a = self.args()
+        return PAGE_RECORDS * max(a.res_stride if self.resident is not None else a.pt_stride, 1)
+
+    @staticmethod
+    def from_workload(w, device="cuda", dev_status: bool = True) -> "Problem":
+        """Copies a host workload (synth.Workload) to the device."""
+        def t(x, dtype=None):
+            if x is None:
+                return None
+            return torch.from_numpy(x).to(device=device, dtype=dtype) if dtype else torch.from_numpy(x).to(device)
+
+        q = torch.from_numpy(w.q.view("int16")).to(device).view(torch.bfloat16)
+        return Problem(
+            q=q, fused_w=t(w.fused_w), kv=t(w.kv), page_table=t(w.page_table), q_len=t(w.q_len),
+            q_req=t(w.q_req), resident=t(w.resident), n_resident=t(w.n_resident),
+            dev_status=torch.zeros(1, dtype=torch.int32, device=device) if dev_status else None)
+
+
+def workspace_bytes(problem_or_args, k: int) -> int:
+    a = problem_or_args.args() if isinstance(problem_or_args, Problem) else problem_or_args
+    return int(load().csa_index_workspace_bytes(ctypes.byref(a), int(k)))
+
+
+def alloc_workspace(problem: Problem, k: int, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(problem, k)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def csa_index_score(problem: Problem, scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Scores of every visible record; invisible columns keep their initial value (NaN)."""
+    a = problem.args()
+    if scores is None:
+        scores = torch.full((problem.num_q, problem.score_stride()), float("nan"), dtype=torch.float32,
+                            device=problem.q_len.device)
+    st = load().csa_index_score(ctypes.byref(a), scores.data_ptr(), int(scores.stride(0)), _stream(stream))
+    _check(st, "csa_index_score")
+    return scores
+
+
+def csa_index_score_topk_fused(problem: Problem, k: int = 512, ws: Optional[torch.Tensor] = None,
+                               idx: Optional[torch.Tensor] = None, vals: Optional[torch.Tensor] = None,
+                               stream=None):
+    """Fused score + top-k. Returns (idx int32 [num_q, k], vals fp32 [num_q, k])."""
+    a = problem.args()
+    dev = problem.q_len.device
+    if ws is None:
+        ws = alloc_workspace(problem, k, dev)
+    if idx is None:
+        idx = torch.empty((problem.num_q, k), dtype=torch.int32, device=dev)
+    if vals is None:
+        vals = torch.empty((problem.num_q, k), dtype=torch.float32, device=dev)
+    st = load().csa_index_score_topk_fused(ctypes.byref(a), int(k), idx.data_ptr(), vals.data_ptr(),
+                                           ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "csa_index_score_topk_fused")
+    return idx, vals
+
+
+def csa_index_topk(scores: torch.Tensor, problem: Problem, k: int = 512, ws: Optional[torch.Tensor] = None,
+                   idx: Optional[torch.Tensor] = None, vals: Optional[torch.Tensor] = None, stream=None):
+    """Top-k over a score matrix laid out as csa_index_score writes it."""
+    a = problem.args()
+    dev = problem.q_len.device
+    if ws is None:
+        ws = alloc_workspace(problem, k, dev)
+    if idx is None:
+        idx = torch.empty((problem.num_q, k), dtype=torch.int32, device=dev)
+    if vals is None:
+        vals = torch.empty((problem.num_q, k), dtype=torch.float32, device=dev)
+    st = load().csa_index_topk(scores.data_ptr(), int(scores.stride(0)), ctypes.byref(a), int(k), idx.data_ptr(),
+                               vals.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "csa_index_topk")
+    return idx, vals

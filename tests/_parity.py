@@ -1,0 +1,78 @@
+"""Comparison of the CUDA path with the oracle.
+
+Tolerances:
+  SCORE_TOL = 2e-3 absolute on scores, and the top-k set rule: the two top-k
+  sets may differ only in records whose oracle score is within SCORE_TOL of the
+  oracle's k-th score (the acceptance bar of the method's parity target).
+  STRICT_SCORE_TOL and STRICT_LOGIT_TOL are this build's tighter internal bars:
+  q is carried exactly through a two-term e4m3 split and the keys are exact, so
+  the remaining error is fp32 accumulation (about 1e-6 relative on a logit).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+SCORE_TOL = 2e-3
+STRICT_SCORE_TOL = 2e-5
+STRICT_LOGIT_TOL = 1e-4  # relative: |dlogit| <= tol * (1 + |logit|)
+
+
+def sigmoid(x):
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-np.asarray(x, dtype=np.float64)))
+
+
+def check_scores(w, gpu_scores: np.ndarray, rows=None):
+    """gpu_scores [num_q, stride] from csa_index_score (NaN where never written)."""
+    P = oracle.Problem(w)
+    o_sc, valid, _ = oracle.scores(P, gpu_scores.shape[1])
+    rows = range(w.num_q) if rows is None else rows
+    for b in rows:
+        v = valid[b]
+        g = gpu_scores[b].astype(np.float64)
+        assert np.all(np.isnan(g[~v])), f"row {b}: columns of invisible records were written"
+        d = np.abs(g[v] - o_sc[b, v])
+        assert not np.any(np.isnan(g[v])), f"row {b}: visible column left unwritten"
+        assert d.max(initial=0.0) <= SCORE_TOL, f"row {b}: max |dscore| {d.max()}"
+        assert d.max(initial=0.0) <= STRICT_SCORE_TOL, f"row {b}: max |dscore| {d.max()} (strict)"
+
+
+def check_topk(w, gpu_idx: np.ndarray, gpu_vals: np.ndarray, k: int, ranked_by_logit: bool = True,
+               oracle_result=None):
+    """Set rule + value check of a GPU top-k against the oracle."""
+    P = oracle.Problem(w)
+    o_idx, o_sc, o_lg, _ = oracle_result if oracle_result is not None else oracle.topk(P, k)
+    assert gpu_idx.shape == (w.num_q, k) and gpu_vals.shape == (w.num_q, k)
+    for b in range(w.num_q):
+        n = int((o_idx[b] >= 0).sum())
+        gi, gv = gpu_idx[b], gpu_vals[b].astype(np.float64)
+        # padding: exactly the tail past the number of visible records
+        assert np.all(gi[:n] >= 0) and np.all(gi[n:] == -1), f"row {b}: padding ({n} visible)"
+        assert np.all(gv[n:] == 0.0), f"row {b}: padding values"
+        if n == 0:
+            continue
+        assert len(set(gi[:n].tolist())) == n, f"row {b}: duplicate positions"
+        # order: non-increasing values
+        assert np.all(np.diff(gv[:n]) <= 0.0), f"row {b}: values not sorted"
+        so, sg = set(o_idx[b, :n].tolist()), set(gi[:n].tolist())
+        s_k, l_k = o_sc[b, n - 1], o_lg[b, n - 1]
+        logit_of = dict(zip(o_idx[b, :n].tolist(), o_lg[b, :n].tolist()))
+        for pos in sg - so:
+            logit_of[pos] = oracle.logit(P, b, pos)
+        for pos in so ^ sg:
+            lg = logit_of[pos]
+            assert abs(sigmoid(lg) - s_k) <= SCORE_TOL, f"row {b}: {pos} differs outside the band"
+            assert abs(lg - l_k) <= STRICT_LOGIT_TOL * (1 + abs(l_k)), \
+                f"row {b}: {pos} differs outside the strict logit band ({lg} vs k-th {l_k})"
+        want = sigmoid(np.array([logit_of[int(p)] for p in gi[:n]]))
+        d = np.abs(gv[:n] - want)
+        assert d.max() <= SCORE_TOL, f"row {b}: max |dval| {d.max()}"
+        assert d.max() <= STRICT_SCORE_TOL, f"row {b}: max |dval| {d.max()} (strict)"
+
+
+def check_exact_topk(w, gpu_idx, k, oracle_result=None):
+    """Exact equality of the returned positions (cases without near-ties)."""
+    o_idx = (oracle_result if oracle_result is not None else oracle.topk(oracle.Problem(w), k))[0]
+    assert np.array_equal(gpu_idx, o_idx)

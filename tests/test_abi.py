@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol the
+header declares, the ctypes mirror matches the C struct layout, the workspace
+size is pure arithmetic and bad host arguments are rejected before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sparse_attention_kv_e4m3_gb300 import build, native
+
+HEADER = os.path.join(build.INCLUDE, "csa_index.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return native.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"csa_index_score", "csa_index_topk", "csa_index_score_topk_fused", "csa_index_workspace_bytes",
+            "csa_status_str", "csa_index_abi_version"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_struct_layout_matches_header(tmp_path):
+    fields = [f[0] for f in native.Args._fields_]
+    src = tmp_path / "layout.c"
+    body = "".join(f'printf("{f} %zu\\n", offsetof(csa_index_args, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "csa_index.h"\n'
+                   'int main(void){' + body + 'printf("sizeof %zu\\n", sizeof(csa_index_args));return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", f"-I{build.INCLUDE}", "-o", str(exe), str(src)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    for f in fields:
+        assert int(got[f]) == getattr(native.Args, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(native.Args)
+
+
+def test_version_and_strings(lib):
+    assert lib.csa_index_abi_version() == 1
+    for s in range(6):
+        assert native.status_str(s)
+    assert native.status_str(99) == "unknown status"
+
+
+def test_workspace_bytes_is_host_arithmetic(lib):
+    a = native.Args()
+    a.num_q = 64
+    slots = 64 + native.MAX_CTAS
+    assert native.workspace_bytes(a, 512) == 512 + slots * (16 + 8 * 512)
+    assert native.workspace_bytes(a, 0) == 0
+    assert native.workspace_bytes(a, native.MAX_K + 1) == 0
+    a.num_q = -1
+    assert native.workspace_bytes(a, 8) == 0
+
+
+def _fake_args(**kw):
+    """Host-side args with well-aligned fake device addresses: validation only."""
+    a = native.Args()
+    a.q, a.fused_w, a.kv, a.page_table, a.q_len = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    a.num_q, a.num_heads, a.head_dim = 4, 64, 128
+    a.num_pages, a.page_stride_bytes = 16, native.PAGE_BYTES
+    a.num_req, a.pt_stride = 4, 4
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("change,want", [
+    (dict(head_dim=64), 2), (dict(num_heads=128), 2), (dict(q=0), 1), (dict(q=0x10008), 3),
+    (dict(kv=0x30004), 3), (dict(page_stride_bytes=8440), 1), (dict(page_stride_bytes=8456), 3),
+    (dict(num_q=-1), 1), (dict(reserved0=1), 1), (dict(q_len=0), 1), (dict(num_req=2), 1),
+    (dict(resident=0x60000), 1), (dict(num_pages=0), 1), (dict(page_table=0x40002), 3),
+])
+def test_score_rejects_bad_args(lib, change, want):
+    a = _fake_args(**change)
+    st = lib.csa_index_score(ctypes.byref(a), ctypes.c_void_p(0x70000), 256, None)
+    assert st == want, (change, st)
+
+
+def test_topk_rejects_bad_args(lib):
+    a = _fake_args()
+    ws = native.workspace_bytes(a, 512)
+    f = lib.csa_index_score_topk_fused
+    assert f(ctypes.byref(a), 0, 0x1000, 0x2000, 0x3000, ws, None) == 1            # k = 0
+    assert f(ctypes.byref(a), 2048, 0x1000, 0x2000, 0x3000, ws, None) == 1         # k too large
+    assert f(ctypes.byref(a), 512, 0x1000, 0x2000, 0x3000, ws - 1, None) == 4      # workspace too small
+    assert f(ctypes.byref(a), 512, 0x1000, 0x2000, None, ws, None) == 4            # no workspace
+    assert f(ctypes.byref(a), 512, 0x1000, 0x2000, 0x3008, ws, None) == 3          # misaligned workspace
+    assert f(ctypes.byref(a), 512, 0x1002, 0x2000, 0x3000, ws, None) == 3          # misaligned idx
+    t = lib.csa_index_topk
+    assert t(0x5000, 128, ctypes.byref(a), 512, 0x1000, 0x2000, 0x3000, ws, None) == 1  # stride < 64*pt_stride
+    assert t(None, 256, ctypes.byref(a), 512, 0x1000, 0x2000, 0x3000, ws, None) == 1
+    assert lib.csa_index_score(None, 0x1000, 256, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    a = _fake_args(num_q=0)
+    assert lib.csa_index_score(ctypes.byref(a), None, 0, None) == 0
+    assert lib.csa_index_score_topk_fused(ctypes.byref(a), 512, None, None, None, 0, None) == 0
