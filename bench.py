@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Benchmark of the fused CSA indexer (score + top-512) on GB300.
+
+One step = one call of csa_index_score_topk_fused over one decode batch: every
+visible record of every query is scored against the FP8 compressed-K cache and
+each query keeps its top-512 (scoring kernel + merge kernel). The default
+workload is the long ragged decode batch: 64 queries, 65536..131072 compressed
+records each (256K-512K tokens at 4:1), shuffled 64-record pages, 5% of records
+with 8x scale outliers, seed 0. Its ~830 MB of keys per step are larger than
+L2, so no flush is needed between steps.
+
+Prints one JSON line. `--impl reference` times the fp64 CPU oracle instead
+(the reference arm). Under torchrun each rank scores its own batch (seed =
+rank): weak scaling, no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA indexer keys scored/s and HBM GB/s (fraction of peak), score+top-512"
+UNIT = "keys/s"
+K_TOP = 512
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_long_ragged_decode.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "sparse_attention_kv_e4m3_gb300", "csrc", f)
+                  for f in ("csa_index.cu", "csa_ptx.cuh", "csa_select.cuh")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the scoring kernel from the committed ncu summary,
+    or None if the kernel sources changed since that capture."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes the step must move at minimum: 132 per visible record, 4 per
+    page-table (and resident-list) entry, 16 KiB of q, 256 B of head weights and
+    4 B of length per query, and the k x (4 + 4) output per query."""
+    vis = w.visible_counts()
+    pages = (vis + 63) // 64
+    per_entry = 8 if w.resident is not None else 4
+    return int((vis * 132).sum() + (pages * per_entry).sum()
+               + w.num_q * (64 * 128 * 2 + 64 * 4 + 4 + K_TOP * 8))
+
+
+# ---------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        self.t0 = time.time()
+        try:
+            self.p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- oracle (reference arm / CPU baseline)
+
+def oracle_rate(w, budget_s: float, min_records: int = 4096):
+    """Times the oracle's top-512 on a bounded prefix sample of every row;
+    returns (keys/s, records scored, seconds, threads, sample text)."""
+    import oracle
+
+    oracle.build()
+    P = oracle.Problem(w)
+    t = time.perf_counter()
+    _, _, n0 = oracle.topk_sample(P, 0, min(4, w.num_q), min_records, K_TOP)
+    dt0 = max(time.perf_counter() - t, 1e-6)
+    rate0 = n0 / dt0
+    per_row = int(max(min_records, min(int(w.visible_counts().max()), rate0 * budget_s / w.num_q)))
+    t = time.perf_counter()
+    _, _, n = oracle.topk_sample(P, 0, w.num_q, per_row, K_TOP)
+    dt = time.perf_counter() - t
+    sample = f"the first {per_row} visible records of each of the {w.num_q} rows ({n} records), top-{K_TOP}"
+    return n / dt, n, dt, oracle.threads(), sample
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    from sparse_attention_kv_e4m3_gb300 import synth
+    import oracle
+
+    oracle.build()
+    w = synth.config(args.workload, seed=0)
+    P = oracle.Problem(w)
+    # size each step so that warmup + steps fit in about two minutes
+    t = time.perf_counter()
+    _, _, n0 = oracle.topk_sample(P, 0, 1, 8192, K_TOP)
+    rate = n0 / max(time.perf_counter() - t, 1e-6)
+    per_step = max(4096, int(rate * 120.0 / max(args.steps + args.warmup, 1)))
+    per_row = max(64, min(int(w.visible_counts().max()), per_step // w.num_q))
+    for _ in range(args.warmup):
+        oracle.topk_sample(P, 0, w.num_q, per_row, K_TOP)
+    times, total = [], 0
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        _, _, n = oracle.topk_sample(P, 0, w.num_q, per_row, K_TOP)
+        times.append(time.perf_counter() - t)
+        total += n
+    value = total / sum(times)
+    sample = f"each step: the first {per_row} visible records of each of the {w.num_q} rows, top-{K_TOP}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "k": K_TOP, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------- native arm
+
+def run_native(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from sparse_attention_kv_e4m3_gb300 import build, native, synth
+
+    build.build()
+    native.load()
+    w = synth.config(args.workload, seed=rank)
+    prob = native.Problem.from_workload(w, device=dev)
+    k = K_TOP
+    ws = native.alloc_workspace(prob, k, dev)
+    idx = torch.empty((w.num_q, k), dtype=torch.int32, device=dev)
+    vals = torch.empty((w.num_q, k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    keys = int(w.visible_counts().sum())
+    alg_bytes = algorithmic_bytes(w)
+
+    def step(mark=None):
+        native.csa_index_score_topk_fused(prob, k, ws, idx, vals, stream=stream, mark=mark)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(prob.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(prob.dev_status.item())} after warm-up")
+
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except Exception:
+        pass
+    sampler = ClockSampler(bus)
+    time.sleep(0.3)
+
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    starts, mids, ends = [E() for _ in range(args.steps)], [E() for _ in range(args.steps)], \
+        [E() for _ in range(args.steps)]
+    e0, e1 = E(), E()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(mark=mids[i])
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    # keep the same load running until the clock sampler has seen at least ~1 s of it
+    extra = 0
+    while time.perf_counter() - t_wall < 1.2:
+        step()
+        extra += 1
+        if extra % 50 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if extra:
+        clocks["window"] = f"timed region ({wall:.3f} s) plus {extra} identical untimed steps"
+
+    ms_total = e0.elapsed_time(e1)
+    ms_step = ms_total / args.steps
+    phase1_ms = statistics.mean(starts[i].elapsed_time(mids[i]) for i in range(args.steps))
+    status = int(prob.dev_status.item())
+
+    keys_all, ms_max = keys, ms_step
+    if dist:
+        t = torch.tensor([float(keys), ms_step], dtype=torch.float64, device=dev)
+        kk = t[:1].clone()
+        dist.all_reduce(kk, op=dist.ReduceOp.SUM)
+        mm = t[1:].clone()
+        dist.all_reduce(mm, op=dist.ReduceOp.MAX)
+        keys_all, ms_max = float(kk.item()), float(mm.item())
+    value = keys_all / (ms_max / 1e3)
+
+    # ---- end to end through the public API: per-step inputs from pinned host memory
+    host = {n: torch.from_numpy(a).pin_memory() for n, a in
+            (("q", w.q.view("int16")), ("fused_w", w.fused_w), ("q_len", w.q_len), ("page_table", w.page_table))}
+    h_idx = torch.empty((w.num_q, k), dtype=torch.int32).pin_memory()
+    h_vals = torch.empty((w.num_q, k), dtype=torch.float32).pin_memory()
+    q16 = prob.q.view(torch.int16)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_idx.numel() * 4 + h_vals.numel() * 4
+
+    def e2e_step():
+        q16.copy_(host["q"], non_blocking=True)
+        prob.fused_w.copy_(host["fused_w"], non_blocking=True)
+        prob.q_len.copy_(host["q_len"], non_blocking=True)
+        prob.page_table.copy_(host["page_table"], non_blocking=True)
+        step()
+        h_idx.copy_(idx, non_blocking=True)
+        h_vals.copy_(vals, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    a0, a1 = E(), E()
+    a0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a0.elapsed_time(a1) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = keys_all / (e2e_ms / 1e3)
+
+    peak, peak_src = measured_peaks()
+    achieved = alg_bytes / (phase1_ms / 1e3) / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": args.workload, "queries": w.num_q, "k": k, "records_per_step": keys,
+                   "records_per_query": "65536..131072" if args.workload == "long_ragged_decode" else None,
+                   "key_bytes_per_step": w.k_bytes(), "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                   "seed": rank},
+        "queries_per_s": w.num_q * world / (ms_max / 1e3),
+        "gbs": alg_bytes * world / (ms_max / 1e3) / 1e9,
+        "roofline": {"kernel": "score_kernel<topk> (scoring phase)", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "phase1_ms": phase1_ms,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "inputs": "q, fused_w, q_len, page_table copied from pinned host memory every step; "
+                          "the compressed-K cache stays resident in HBM",
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "device_status": status,
+        "wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, dt, threads, sample = oracle_rate(w, budget_s=10.0)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": sample, "seconds": dt,
+                                "affinity_cores": len(os.sched_getaffinity(0))}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="long_ragged_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -182,6 +182,16 @@ csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_i
 csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int32_t* idx,
                                       float* vals, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * csa_index_score_topk_fused with one addition for profiling: `event` (a
+ * cudaEvent_t passed as void*, or NULL) is recorded on `stream` between the
+ * scoring kernel and the merge kernel, so a caller can time the two apart with
+ * events of its own before and after the call. Same results and errors as
+ * csa_index_score_topk_fused; CSA_ERR_CUDA if recording the event fails.
+ */
+csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t k, int32_t* idx, float* vals,
+                                             void* ws, size_t ws_bytes, void* stream, void* event);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1043,6 +1043,11 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
 
 csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int32_t* idx, float* vals, void* ws,
                                       size_t ws_bytes, void* stream) {
+  return csa_index_score_topk_fused_marked(args, k, idx, vals, ws, ws_bytes, stream, nullptr);
+}
+
+csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t k, int32_t* idx, float* vals,
+                                             void* ws, size_t ws_bytes, void* stream, void* event) {
   csa_status st = check_args(args, kNeedQ | kNeedKv);
   if (st != CSA_OK) return st;
   if (k < 1 || k > CSA_MAX_K) return CSA_ERR_INVALID_ARG;
@@ -1062,6 +1067,7 @@ csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   score_kernel<true><<<sms, kThreads, kSmemBytes, s>>>(P);
   if ((st = launch_status()) != CSA_OK) return st;
+  if (event && cudaEventRecord(static_cast<cudaEvent_t>(event), s) != cudaSuccess) return CSA_ERR_CUDA;
   merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
   return launch_status();
 }

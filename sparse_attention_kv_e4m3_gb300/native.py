@@ -87,6 +87,8 @@ def load(path: Optional[str] = None):
             lib.csa_index_topk.restype = ctypes.c_int
             lib.csa_index_score_topk_fused.argtypes = [A, i32, vp, vp, vp, sz, vp]
             lib.csa_index_score_topk_fused.restype = ctypes.c_int
+            lib.csa_index_score_topk_fused_marked.argtypes = [A, i32, vp, vp, vp, sz, vp, vp]
+            lib.csa_index_score_topk_fused_marked.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -203,8 +205,10 @@ def csa_index_score(problem: Problem, scores: Optional[torch.Tensor] = None, str
 
 def csa_index_score_topk_fused(problem: Problem, k: int = 512, ws: Optional[torch.Tensor] = None,
                                idx: Optional[torch.Tensor] = None, vals: Optional[torch.Tensor] = None,
-                               stream=None):
-    """Fused score + top-k. Returns (idx int32 [num_q, k], vals fp32 [num_q, k])."""
+                               stream=None, mark: Optional[torch.cuda.Event] = None):
+    """Fused score + top-k. Returns (idx int32 [num_q, k], vals fp32 [num_q, k]).
+
+    `mark`, when given, is recorded between the scoring and the merge kernel."""
     a = problem.args()
     dev = problem.q_len.device
     if ws is None:
@@ -213,8 +217,16 @@ def csa_index_score_topk_fused(problem: Problem, k: int = 512, ws: Optional[torc
         idx = torch.empty((problem.num_q, k), dtype=torch.int32, device=dev)
     if vals is None:
         vals = torch.empty((problem.num_q, k), dtype=torch.float32, device=dev)
-    st = load().csa_index_score_topk_fused(ctypes.byref(a), int(k), idx.data_ptr(), vals.data_ptr(),
-                                           ws.data_ptr(), ws.numel(), _stream(stream))
+    if mark is None:
+        st = load().csa_index_score_topk_fused(ctypes.byref(a), int(k), idx.data_ptr(), vals.data_ptr(),
+                                               ws.data_ptr(), ws.numel(), _stream(stream))
+    else:
+        # torch only lets elapsed_time() read events it recorded itself: record once
+        # here; the library records the same event again between its two kernels.
+        mark.record(torch.cuda.current_stream() if stream is None else stream)
+        st = load().csa_index_score_topk_fused_marked(ctypes.byref(a), int(k), idx.data_ptr(), vals.data_ptr(),
+                                                      ws.data_ptr(), ws.numel(), _stream(stream),
+                                                      ctypes.c_void_p(mark.cuda_event))
     _check(st, "csa_index_score_topk_fused")
     return idx, vals
 

@@ -64,8 +64,12 @@ def check_topk(w, gpu_idx: np.ndarray, gpu_vals: np.ndarray, k: int, ranked_by_l
         for pos in so ^ sg:
             lg = logit_of[pos]
             assert abs(sigmoid(lg) - s_k) <= SCORE_TOL, f"row {b}: {pos} differs outside the band"
-            assert abs(lg - l_k) <= STRICT_LOGIT_TOL * (1 + abs(l_k)), \
-                f"row {b}: {pos} differs outside the strict logit band ({lg} vs k-th {l_k})"
+            # A path that ranks fp32 scores cannot separate logits whose sigmoids round to
+            # the same fp32 value (every logit above ~17 is 1.0f), so the logit band only
+            # binds the logit-ranked fused path.
+            if ranked_by_logit:
+                assert abs(lg - l_k) <= STRICT_LOGIT_TOL * (1 + abs(l_k)), \
+                    f"row {b}: {pos} differs outside the strict logit band ({lg} vs k-th {l_k})"
         want = sigmoid(np.array([logit_of[int(p)] for p in gi[:n]]))
         d = np.abs(gv[:n] - want)
         assert d.max() <= SCORE_TOL, f"row {b}: max |dval| {d.max()}"
