@@ -132,6 +132,38 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------- ranks
+
+def reduce_over_ranks(keys: float, ms_step: float, dist=None, device=None):
+    """Whole-job throughput inputs: keys summed over ranks, step time maxed over
+    ranks (every rank scores its own independent batch)."""
+    if dist is None:
+        return float(keys), float(ms_step)
+    import torch
+
+    k = torch.tensor([float(keys)], dtype=torch.float64, device=device)
+    m = torch.tensor([float(ms_step)], dtype=torch.float64, device=device)
+    dist.all_reduce(k, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(k.item()), float(m.item())
+
+
+def merge_shard_topk(shards, k: int):
+    """Exact top-k of one row from per-shard top-k lists [(positions, logits), ...]
+    (context-parallel scoring: each shard holds some of the row's pages). The global
+    top-k is contained in the union of the local ones; ties rank lower positions first."""
+    pos = np.concatenate([np.asarray(p, dtype=np.int64) for p, _ in shards])
+    lg = np.concatenate([np.asarray(v, dtype=np.float64) for _, v in shards])
+    keep = pos >= 0
+    pos, lg = pos[keep], lg[keep]
+    order = np.lexsort((pos, -lg))[:k]
+    out_p = np.full(k, -1, dtype=np.int64)
+    out_l = np.full(k, -np.inf)
+    out_p[: len(order)] = pos[order]
+    out_l[: len(order)] = lg[order]
+    return out_p, out_l
+
+
 # ---------------------------------------------------------------------- oracle (reference arm / CPU baseline)
 
 def oracle_rate(w, budget_s: float, min_records: int = 4096):
@@ -274,14 +306,7 @@ def run_native(args):
     phase1_ms = statistics.mean(starts[i].elapsed_time(mids[i]) for i in range(args.steps))
     status = int(prob.dev_status.item())
 
-    keys_all, ms_max = keys, ms_step
-    if dist:
-        t = torch.tensor([float(keys), ms_step], dtype=torch.float64, device=dev)
-        kk = t[:1].clone()
-        dist.all_reduce(kk, op=dist.ReduceOp.SUM)
-        mm = t[1:].clone()
-        dist.all_reduce(mm, op=dist.ReduceOp.MAX)
-        keys_all, ms_max = float(kk.item()), float(mm.item())
+    keys_all, ms_max = reduce_over_ranks(keys, ms_step, dist, dev)
     value = keys_all / (ms_max / 1e3)
 
     # ---- end to end through the public API: per-step inputs from pinned host memory
@@ -314,10 +339,7 @@ def run_native(args):
     a1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = a0.elapsed_time(a1) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    _, e2e_ms = reduce_over_ranks(0.0, e2e_ms, dist, dev)
     e2e_value = keys_all / (e2e_ms / 1e3)
 
     peak, peak_src = measured_peaks()

@@ -56,24 +56,33 @@ constexpr int kRec = 132;
 constexpr int kPageBytes = kPage * kRec;  // 8448
 constexpr int kTile = 128;                // records per MMA tile (two pages)
 
-constexpr int kStages = 12;  // page stages in shared memory
-constexpr int kAStages = 4;  // TMEM A (key tile) stages
-constexpr int kDStages = 4;  // TMEM accumulator stages
-constexpr int kRing = 4;     // page-walker ring slots of 32 pages
-constexpr int kCap = 4096;   // candidate buffer of one segment (keys)
+constexpr int kStages = 12;    // page stages in shared memory
+constexpr int kAStages = 4;    // TMEM A (key tile) stages
+constexpr int kDStages = 3;    // TMEM accumulator stages (128 fp32 columns each)
+constexpr int kRing = 4;       // page-walker ring slots of 32 pages
+constexpr int kCap = 4096;     // candidate buffer of one segment (keys)
+constexpr int kKeyRing = 16;   // tiles of ranking keys between the workers and the selector
 
-constexpr int kThreads = 384;
-constexpr int kWarpIssuer = 0, kWarpMma = 1, kWarpWalker = 2, kWarpQprep = 3, kWarpLoader = 4, kWarpEpi = 8;
-constexpr int kBarLoader = 1, kBarEpi = 2;
+constexpr int kThreads = 512;
+// warp roles
+constexpr int kWarpIssuer = 0, kWarpMma = 1, kWarpWalker = 2, kWarpQprep = 3;
+constexpr int kWarpWorker = 4;   // warps 4-7: worker group 0 (even tiles), 8-11: group 1 (odd tiles)
+constexpr int kWorkerGroups = 2;
+constexpr int kWarpSelect = 12;  // warps 12-15: top-k selector
+constexpr int kBarSelect = 1;
+constexpr int kQEmptyCount = 1 + 4 * kWorkerGroups;  // MMA commit + every worker warp
 
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t a_col(int s) { return static_cast<uint32_t>(s) * 32u; }
-__host__ __device__ constexpr uint32_t d_col(int s) { return 128u + static_cast<uint32_t>(s) * 64u; }
-__host__ __device__ constexpr uint32_t si_col(int s) { return 384u + static_cast<uint32_t>(s) * 2u; }
-static_assert(si_col(kDStages) <= kTmemCols, "TMEM column map");
+__host__ __device__ constexpr uint32_t d_col(int s) { return 128u + static_cast<uint32_t>(s) * 128u; }
+static_assert(d_col(kDStages) <= kTmemCols, "TMEM column map");
 static_assert(a_col(kAStages) <= d_col(0), "TMEM column map");
+static_assert(kAStages == 2 * kWorkerGroups, "each worker group loads two own tiles ahead");
 
-constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 64);
+// B = the query's two e4m3 terms stacked as 128 rows (hi: heads 0-63, lo: heads
+// 0-63 again), so one N = 128 MMA yields both partial dots of every head; an
+// N = 128 MMA with A in TMEM costs the same issue time as N = 64.
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
 constexpr uint32_t kNaNBits = 0x7FC00000u;
 
 struct Params {
@@ -290,6 +299,7 @@ struct __align__(1024) Smem {
   uint8_t pages[kStages][kPageBytes];
   uint64_t cand[kCap];
   uint64_t scratch[CSA_MAX_K];
+  uint64_t keys[kKeyRing][kTile];  // ranking keys of one tile, worker -> selector
   float wbuf[2][kH];
   PageInfo ring[kRing * 32];
   PageInfo info[kStages];
@@ -298,6 +308,7 @@ struct __align__(1024) Smem {
   uint64_t dfull[kDStages], dempty[kDStages];
   uint64_t qfull[2], qempty[2];
   uint64_t rfull[kRing], rempty[kRing];
+  uint64_t kfull[kKeyRing], kempty[kKeyRing];
   uint64_t drain;
   SelectShared sel;
   Plan plan;
@@ -305,7 +316,7 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t status;
-  int32_t go[2][2];                // [group][iteration parity] broadcast of a leader's wait result
+  int32_t go[2];                   // selector leader's wait result, by tile parity
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
@@ -417,14 +428,9 @@ __device__ void role_mma(const Params& P, Smem& S) {
     tc_fence_after();
     const uint32_t dt = tmem + d_col(td);
     const uint32_t at = tmem + a_col(ta);
+    const uint32_t bq = smem_u32(S.qbuf[qs][0]);  // 128 rows: [hi | lo]
 #pragma unroll
-    for (int term = 0; term < 2; ++term) {
-      const uint32_t bq = smem_u32(S.qbuf[qs][term]);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc, (term | kk) != 0);
-      }
-    }
+    for (int kk = 0; kk < 4; ++kk) mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc, kk != 0);
     mma_commit(smem_u32(&S.aempty[ta]));
     mma_commit(smem_u32(&S.dfull[td]));
     const bool seg_end = (i == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
@@ -516,39 +522,49 @@ __device__ void role_qprep(const Params& P, Smem& S) {
   if (lane == 0 && flags) atomicOr(&S.status, flags);
 }
 
-__device__ void role_loader(const Params& P, Smem& S) {
-  const int g = threadIdx.x - kWarpLoader * 32;  // 0..127
-  const int q = g >> 5, lane = g & 31;
-  const int half = q >> 1;
-  const int r = g & 63;
+// Broadcast of lane 0's value to the warp.
+__device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0; }
+
+// One warp of a worker group: TMEM lane quarter q of every tile the group owns
+// (tiles i with i % kWorkerGroups == group). For each own tile it first moves
+// its 32 records' key bytes from the staged page into the TMEM A operand
+// ("load", two own tiles ahead of the epilogue) and later turns the MMA's head
+// dots into logits ("epilogue"). The warps never wait on each other.
+template <bool kTopk>
+__device__ void role_worker(const Params& P, Smem& S) {
+  const int wi = (threadIdx.x >> 5) - kWarpWorker;
+  const int group = wi >> 2;
+  const int q = wi & 3;
+  const int lane = threadIdx.x & 31;
+  const int half = q >> 1;                 // page of the tile this quarter reads
+  const int r = 32 * (q & 1) + lane;       // record row inside that page
+  const int row = 32 * q + lane;           // record row inside the tile
   const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
   const uint32_t tmem = S.tmem_base;
-  for (int64_t i = 0; i < S.plan.ntiles; ++i) {
-    const int ta = static_cast<int>(i % kAStages), td = static_cast<int>(i % kDStages);
-    const int64_t pg0 = 2 * i;
-    const int s0 = static_cast<int>(pg0 % kStages), s1 = static_cast<int>((pg0 + 1) % kStages);
-    const uint32_t ph0 = static_cast<uint32_t>((pg0 / kStages) & 1), ph1 = static_cast<uint32_t>(((pg0 + 1) / kStages) & 1);
-    if (g == 0) {
-      const bool ok =
-          mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag) &&
-          mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((i / kDStages) & 1) ^ 1), &S.abort_flag) &&
-          mbar_wait(smem_u32(&S.full[s0]), ph0, &S.abort_flag) && mbar_wait(smem_u32(&S.full[s1]), ph1, &S.abort_flag);
-      S.go[0][i & 1] = ok ? 1 : 0;
-    }
-    named_bar_sync(kBarLoader, 128);
-    if (!S.go[0][i & 1]) break;
-    const int s = half ? s1 : s0;
-    mbar_wait_drain(smem_u32(&S.full[s]), half ? ph1 : ph0);  // already complete: acquire for this thread
+  const int64_t nt = S.plan.ntiles;
+
+  // Loads own tile i. Returns false on abort; scale bits (NaN when the record
+  // is not visible) and the record's logical position come back in sc / pos.
+  auto load = [&](int64_t i, uint32_t& sc, uint32_t& pos) -> bool {
+    const int ta = static_cast<int>(i % kAStages);
+    const int64_t pg = 2 * i + half;
+    const int s = static_cast<int>(pg % kStages);
+    const uint32_t ph = static_cast<uint32_t>((pg / kStages) & 1);
+    bool ok = true;
+    if (lane == 0)
+      ok = mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag) &&
+           mbar_wait(smem_u32(&S.full[s]), ph, &S.abort_flag);
+    if (!warp_ok(ok)) return false;
+    mbar_wait_drain(smem_u32(&S.full[s]), ph);  // complete already: acquire for this lane
     const PageInfo e = S.info[s];
     const uint8_t* src = S.pages[s] + r * kRec;
     uint32_t v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = *reinterpret_cast<const uint32_t*>(src + 4 * j);
-    const uint32_t sc = *reinterpret_cast<const uint32_t*>(src + kD);
-    const bool valid = r < e.nrows;
+    const uint32_t scale = *reinterpret_cast<const uint32_t*>(src + kD);
+    sc = r < e.nrows ? scale : kNaNBits;
+    pos = static_cast<uint32_t>(e.lp * kPage + r);
     tmem_st32(tmem + a_col(ta) + lane_off, v);
-    tmem_st2(tmem + si_col(td) + lane_off, valid ? sc : kNaNBits,
-             static_cast<uint32_t>(e.lp * kPage + r));
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -556,117 +572,147 @@ __device__ void role_loader(const Params& P, Smem& S) {
       mbar_arrive(smem_u32(&S.empty[s]));
       mbar_arrive(smem_u32(&S.afull[ta]));
     }
-  }
-}
+    return true;
+  };
 
-template <bool kTopk>
-__device__ void role_epilogue(const Params& P, Smem& S) {
-  const int g = threadIdx.x - kWarpEpi * 32;  // 0..127
-  const int q = g >> 5, lane = g & 31;
-  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t tmem = S.tmem_base;
-  Cursor cur;
-  cur.init(P, S.plan);
-  int seg = 0;
-  float w[kH];
-  for (int64_t i = 0; i < S.plan.ntiles; ++i) {
-    const bool seg_start = (i == 0) || (cur.lt == 0);
-    if (seg_start && i > 0) ++seg;
-    const int qs = seg & 1;
+  // Epilogue of own tile i of row b, local tile lt, segment `seg`.
+  auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, uint32_t sc, uint32_t pos) -> bool {
     const int td = static_cast<int>(i % kDStages);
-    const uint32_t qph = static_cast<uint32_t>((seg >> 1) & 1);
     const uint32_t dph = static_cast<uint32_t>((i / kDStages) & 1);
-    if (g == 0) {
-      const bool ok = (!seg_start || mbar_wait(smem_u32(&S.qfull[qs]), qph, &S.abort_flag)) &&
-                      mbar_wait(smem_u32(&S.dfull[td]), dph, &S.abort_flag);
-      S.go[1][i & 1] = ok ? 1 : 0;
-    }
-    named_bar_sync(kBarEpi, 128);
-    if (!S.go[1][i & 1]) break;
-    if (seg_start) {
-      mbar_wait_drain(smem_u32(&S.qfull[qs]), qph);
-#pragma unroll
-      for (int h = 0; h < kH; ++h) w[h] = S.wbuf[qs][h];
-    }
-    mbar_wait_drain(smem_u32(&S.dfull[td]), dph);
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(smem_u32(&S.dfull[td]), dph, &S.abort_flag);
+    if (!warp_ok(ok)) return false;
+    __syncwarp();
     tc_fence_after();
-    uint32_t x0[32], x1[32];
-    uint32_t sc_bits, pos_bits;
-    tmem_ld32(tmem + d_col(td) + lane_off, x0);
-    tmem_ld32(tmem + d_col(td) + 32 + lane_off, x1);
-    tmem_ld2(tmem + si_col(td) + lane_off, sc_bits, pos_bits);
-    tmem_wait_ld();
+    // columns 0-63: k . (q_hi * 2^e), 64-127: k . (q_lo * 2^e); a head's dot is their sum
+    const float s = __uint_as_float(sc);
+    const bool valid = !isnan(s);
+    const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // heads 32*part .. 32*part + 31
+      uint32_t hi[32], lo[32];
+      tmem_ld32(tmem + d_col(td) + 32 * part + lane_off, hi);
+      tmem_ld32(tmem + d_col(td) + 64 + 32 * part + lane_off, lo);
+      tmem_wait_ld();
+      // relu(s * x) = s * max(x, 0) for s >= 0 and s * min(x, 0) for s < 0
+      if (s >= 0.0f) {
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          const float4 w = wv[8 * part + (h >> 2)];
+          a0 = fmaf(fmaxf(__uint_as_float(hi[h]) + __uint_as_float(lo[h]), 0.f), w.x, a0);
+          a1 = fmaf(fmaxf(__uint_as_float(hi[h + 1]) + __uint_as_float(lo[h + 1]), 0.f), w.y, a1);
+          a2 = fmaf(fmaxf(__uint_as_float(hi[h + 2]) + __uint_as_float(lo[h + 2]), 0.f), w.z, a2);
+          a3 = fmaf(fmaxf(__uint_as_float(hi[h + 3]) + __uint_as_float(lo[h + 3]), 0.f), w.w, a3);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          const float4 w = wv[8 * part + (h >> 2)];
+          a0 = fmaf(fminf(__uint_as_float(hi[h]) + __uint_as_float(lo[h]), 0.f), w.x, a0);
+          a1 = fmaf(fminf(__uint_as_float(hi[h + 1]) + __uint_as_float(lo[h + 1]), 0.f), w.y, a1);
+          a2 = fmaf(fminf(__uint_as_float(hi[h + 2]) + __uint_as_float(lo[h + 2]), 0.f), w.z, a2);
+          a3 = fmaf(fminf(__uint_as_float(hi[h + 3]) + __uint_as_float(lo[h + 3]), 0.f), w.w, a3);
+        }
+      }
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
-
-    const float s = __uint_as_float(sc_bits);
-    const bool valid = !isnan(s);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    if (s >= 0.0f) {
-#pragma unroll
-      for (int h = 0; h < 32; h += 4) {
-        a0 = fmaf(fmaxf(__uint_as_float(x0[h]), 0.f), w[h], a0);
-        a1 = fmaf(fmaxf(__uint_as_float(x0[h + 1]), 0.f), w[h + 1], a1);
-        a2 = fmaf(fmaxf(__uint_as_float(x0[h + 2]), 0.f), w[h + 2], a2);
-        a3 = fmaf(fmaxf(__uint_as_float(x0[h + 3]), 0.f), w[h + 3], a3);
-      }
-#pragma unroll
-      for (int h = 0; h < 32; h += 4) {
-        a0 = fmaf(fmaxf(__uint_as_float(x1[h]), 0.f), w[32 + h], a0);
-        a1 = fmaf(fmaxf(__uint_as_float(x1[h + 1]), 0.f), w[32 + h + 1], a1);
-        a2 = fmaf(fmaxf(__uint_as_float(x1[h + 2]), 0.f), w[32 + h + 2], a2);
-        a3 = fmaf(fmaxf(__uint_as_float(x1[h + 3]), 0.f), w[32 + h + 3], a3);
-      }
-    } else {
-      // relu(s * x) = s * min(x, 0) for s < 0
-#pragma unroll
-      for (int h = 0; h < 32; h += 4) {
-        a0 = fmaf(fminf(__uint_as_float(x0[h]), 0.f), w[h], a0);
-        a1 = fmaf(fminf(__uint_as_float(x0[h + 1]), 0.f), w[h + 1], a1);
-        a2 = fmaf(fminf(__uint_as_float(x0[h + 2]), 0.f), w[h + 2], a2);
-        a3 = fmaf(fminf(__uint_as_float(x0[h + 3]), 0.f), w[h + 3], a3);
-      }
-#pragma unroll
-      for (int h = 0; h < 32; h += 4) {
-        a0 = fmaf(fminf(__uint_as_float(x1[h]), 0.f), w[32 + h], a0);
-        a1 = fmaf(fminf(__uint_as_float(x1[h + 1]), 0.f), w[32 + h + 1], a1);
-        a2 = fmaf(fminf(__uint_as_float(x1[h + 2]), 0.f), w[32 + h + 2], a2);
-        a3 = fmaf(fminf(__uint_as_float(x1[h + 3]), 0.f), w[32 + h + 3], a3);
-      }
-    }
     const float logit = s * ((a0 + a1) + (a2 + a3));
-    const int32_t pos = static_cast<int32_t>(pos_bits);
 
     if constexpr (!kTopk) {
-      if (valid) {
-        const int64_t col = cur.lt * kTile + g;
-        P.scores[static_cast<int64_t>(cur.b) * P.score_stride + col] = 1.0f / (1.0f + expf(-logit));
-      }
+      if (valid) P.scores[static_cast<int64_t>(b) * P.score_stride + lt * kTile + row] = 1.0f / (1.0f + expf(-logit));
     } else {
-      const uint64_t key = (valid && !isnan(logit)) ? make_key(logit, pos) : 0ull;
-      append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
-      named_bar_sync(kBarEpi, 128);
-      shrink_if_above<128>(S.cand, S.scratch, kCap - 128, P.k, &S.sel, kBarEpi, g);
+      const uint64_t key = (valid && !isnan(logit)) ? make_key(logit, static_cast<int32_t>(pos)) : 0ull;
+      const int slot = static_cast<int>(i % kKeyRing);
+      bool ok2 = true;
+      if (lane == 0)
+        ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
+                        &S.abort_flag);
+      if (!warp_ok(ok2)) return false;
+      S.keys[slot][row] = key;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.kfull[slot]));
     }
+    return true;
+  };
 
-    const bool seg_end = (i == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
-    if (seg_end) {
-      if constexpr (kTopk) {
-        shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, &S.sel, kBarEpi, g);
-        const int n = static_cast<int>(S.sel.n);
-        uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
-        uint64_t* ent = reinterpret_cast<uint64_t*>(slot + 16);
-        for (int j = g; j < n; j += 128) ent[j] = S.cand[j];
-        named_bar_sync(kBarEpi, 128);
-        if (g == 0) {
-          *reinterpret_cast<int32_t*>(slot) = n;
-          S.sel.n = 0;
-          S.sel.tau = 0;
-        }
-        named_bar_sync(kBarEpi, 128);
+  // scale bits and positions of the two own tiles loaded ahead (even / odd own tile)
+  uint32_t sc0 = 0, pos0 = 0, sc1 = 0, pos1 = 0;
+  bool ok = true;
+  // prologue: the group's first two tiles
+  if (group < nt) ok = load(group, sc0, pos0);
+  if (ok && group + kWorkerGroups < nt) ok = load(group + kWorkerGroups, sc1, pos1);
+
+  Cursor cur;
+  cur.init(P, S.plan);
+  int seg = 0, wseg = -1;
+  int64_t mine = 0;  // own tiles finished
+  for (int64_t t = 0; ok && t < nt; ++t) {
+    const bool seg_start = (t == 0) || (cur.lt == 0);
+    if (seg_start && t > 0) ++seg;
+    const bool seg_end = (t == nt - 1) || (cur.lt == cur.tiles - 1);
+    if (t % kWorkerGroups == group) {
+      if (seg != wseg) {  // first own tile of this segment: its head weights must be ready
+        bool okq = true;
+        if (lane == 0)
+          okq = mbar_wait(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag);
+        if (!warp_ok(okq)) break;
+        mbar_wait_drain(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1));
+        wseg = seg;
       }
-      if (g == 0) mbar_arrive(smem_u32(&S.qempty[qs]));
+      if ((mine & 1) == 0) {
+        ok = epilogue(t, cur.b, cur.lt, seg, sc0, pos0);
+        if (ok && t + 2 * kWorkerGroups < nt) ok = load(t + 2 * kWorkerGroups, sc0, pos0);
+      } else {
+        ok = epilogue(t, cur.b, cur.lt, seg, sc1, pos1);
+        if (ok && t + 2 * kWorkerGroups < nt) ok = load(t + 2 * kWorkerGroups, sc1, pos1);
+      }
+      ++mine;
+    }
+    if (seg_end) {  // done with this segment's head weights
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.qempty[seg & 1]));
+    }
+    cur.advance(P);
+  }
+}
+
+// Top-k selector (warps 12-15): takes every tile's 128 keys in tile order,
+// keeps those above the segment's running threshold in a shared-memory
+// buffer, cuts the buffer back to the best k when it fills, and writes each
+// segment's best k to workspace slot (row + CTA).
+__device__ void role_select(const Params& P, Smem& S) {
+  const int g = threadIdx.x - kWarpSelect * 32;
+  Cursor cur;
+  cur.init(P, S.plan);
+  for (int64_t t = 0; t < S.plan.ntiles; ++t) {
+    const int slot = static_cast<int>(t % kKeyRing);
+    const uint32_t ph = static_cast<uint32_t>((t / kKeyRing) & 1);
+    if (g == 0) S.go[t & 1] = mbar_wait(smem_u32(&S.kfull[slot]), ph, &S.abort_flag) ? 1 : 0;
+    named_bar_sync(kBarSelect, 128);
+    if (!S.go[t & 1]) break;
+    mbar_wait_drain(smem_u32(&S.kfull[slot]), ph);
+    const uint64_t key = S.keys[slot][g];
+    append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+    named_bar_sync(kBarSelect, 128);
+    if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
+    shrink_if_above<128>(S.cand, S.scratch, kCap - 128, P.k, &S.sel, kBarSelect, g);
+    const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
+    if (seg_end) {
+      shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, &S.sel, kBarSelect, g);
+      const int n = static_cast<int>(S.sel.n);
+      uint8_t* out = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
+      uint64_t* ent = reinterpret_cast<uint64_t*>(out + 16);
+      for (int j = g; j < n; j += 128) ent[j] = S.cand[j];
+      named_bar_sync(kBarSelect, 128);
+      if (g == 0) {
+        *reinterpret_cast<int32_t*>(out) = n;
+        S.sel.n = 0;
+        S.sel.tau = 0;
+      }
+      named_bar_sync(kBarSelect, 128);
     }
     cur.advance(P);
   }
@@ -696,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
       mbar_init(smem_u32(&S.empty[s]), 2);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(smem_u32(&S.afull[s]), 4);
+      mbar_init(smem_u32(&S.afull[s]), 4);  // the four warps of the loading worker group
       mbar_init(smem_u32(&S.aempty[s]), 1);
     }
     for (int s = 0; s < kDStages; ++s) {
@@ -705,7 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&S.qfull[s]), 1);
-      mbar_init(smem_u32(&S.qempty[s]), 2);
+      mbar_init(smem_u32(&S.qempty[s]), kQEmptyCount);
+    }
+    for (int s = 0; s < kKeyRing; ++s) {
+      mbar_init(smem_u32(&S.kfull[s]), 4);
+      mbar_init(smem_u32(&S.kempty[s]), 1);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(smem_u32(&S.rfull[s]), 1);
@@ -731,10 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
     role_walker(P, S);
   } else if (warp == kWarpQprep) {
     role_qprep(P, S);
-  } else if (warp < kWarpEpi) {
-    role_loader(P, S);
-  } else {
-    role_epilogue<kTopk>(P, S);
+  } else if (warp < kWarpSelect) {
+    role_worker<kTopk>(P, S);
+  } else if (kTopk) {
+    role_select(P, S);
   }
 
   tc_fence_before();
