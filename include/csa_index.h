@@ -192,6 +192,36 @@ csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int
 csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t k, int32_t* idx, float* vals,
                                              void* ws, size_t ws_bytes, void* stream, void* event);
 
+/* Size of the library's built-in scratch used by csa_index_score_topk_fused_static. */
+#define CSA_STATIC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * Fused score + top-k that allocates nothing and needs no workspace from the
+ * caller. No page describes this entry point; it exists for callers that cannot
+ * hand the library device memory of their own: a plain C host without a device
+ * allocator, a plugin whose host application owns every device allocation, or a
+ * decode loop that must not call cudaMalloc (which may synchronise the device)
+ * while it runs. It computes exactly what csa_index_score_topk_fused computes,
+ * with the same argument, idx / vals and error contract, but keeps its scratch
+ * (row tile offsets and per-segment candidate slots) in a CSA_STATIC_SCRATCH_BYTES
+ * array that every GPU loading the library holds until the process exits.
+ *
+ * Limit: the call needs 256-byte-rounded 4*(num_q+1) bytes plus
+ * (num_q + number of SMs) * (16 + 8*k rounded up to 16) bytes of that array
+ * (64 rows at k = 512 on a 152-SM GB300 use about 0.9 MB); larger requests return
+ * CSA_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. Every call on a device uses the same array and
+ * leaves its contents behind; nothing in it has to start at zero, because each
+ * call writes every byte it later reads. Calls whose kernels overlap on the GPU
+ * (two streams, or two host threads) race on the array and must be serialised
+ * by the caller. The library calls no cudaMalloc or cudaFree here.
+ */
+csa_status csa_index_score_topk_fused_static(const csa_index_args* args, int32_t k, int32_t* idx, float* vals,
+                                             void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1153,3 +1153,62 @@ csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_i
 }
 
 }  // extern "C"
+
+// ====================================================================== built-in scratch
+
+// Scratch of csa_index_score_topk_fused_static: the row tile offsets and the
+// per-segment candidate slots that csa_index_score_topk_fused otherwise keeps in
+// the caller's workspace. Every GPU that loads the library holds this array
+// until the process exits; all calls on a device share it.
+static __device__ __align__(256) uint8_t csa_static_scratch[CSA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices];
+
+// Device address of csa_static_scratch on the current device, looked up once per
+// device (host code may not use the symbol itself: it names a host-side shadow).
+csa_status static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, csa_static_scratch) != cudaSuccess || !p) return CSA_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" csa_status csa_index_score_topk_fused_static(const csa_index_args* args, int32_t k, int32_t* idx,
+                                                        float* vals, void* stream) {
+  csa_status st = check_args(args, kNeedQ | kNeedKv);
+  if (st != CSA_OK) return st;
+  if (k < 1 || k > CSA_MAX_K) return CSA_ERR_INVALID_ARG;
+  if (args->num_q == 0) return CSA_OK;
+  if (!idx || !vals) return CSA_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || !aligned(vals, 4)) return CSA_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != CSA_OK) return st;
+  // The scoring kernel writes slot (row + CTA) for CTA < grid = SM count.
+  const size_t need =
+      slots_offset_for(args->num_q) + (static_cast<size_t>(args->num_q) + sms) * slot_bytes_for(k);
+  if (need > CSA_STATIC_SCRATCH_BYTES) return CSA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((st = static_scratch_address(&scratch)) != CSA_OK) return st;
+  Params P = params_of(args);
+  P.ws = static_cast<uint8_t*>(scratch);
+  P.k = k;
+  P.slot_bytes = static_cast<int64_t>(slot_bytes_for(k));
+  P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
+  P.grid = sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  score_kernel<true><<<sms, kThreads, kSmemBytes, s>>>(P);
+  if ((st = launch_status()) != CSA_OK) return st;
+  merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
+  return launch_status();
+}

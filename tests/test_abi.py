@@ -110,6 +110,17 @@ def test_topk_rejects_bad_args(lib):
     assert lib.csa_index_score(None, 0x1000, 256, None) == 1
 
 
+def test_static_scratch_variant_validates_on_the_host(lib):
+    f = lib.csa_index_score_topk_fused_static
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    a = _fake_args()
+    assert f(None, 512, 0x1000, 0x2000, None) == 1
+    assert f(ctypes.addressof(a), 0, 0x1000, 0x2000, None) == 1
+    assert f(ctypes.addressof(a), 512, 0x1002, 0x2000, None) == 3
+    assert f(ctypes.addressof(_fake_args(head_dim=64)), 512, 0x1000, 0x2000, None) == 2
+
+
 def test_empty_batch_is_a_no_op(lib):
     a = _fake_args(num_q=0)
     assert lib.csa_index_score(ctypes.byref(a), None, 0, None) == 0
