@@ -54,14 +54,18 @@ constexpr int kD = 128;
 constexpr int kPage = 64;
 constexpr int kRec = 132;
 constexpr int kPageBytes = kPage * kRec;  // 8448
-constexpr int kTile = 128;                // records per MMA tile (two pages)
+constexpr int kMmaRows = 128;             // records per MMA (M)
+constexpr int kSub = 2;                   // MMA sub-tiles per tile
+constexpr int kTile = kSub * kMmaRows;    // records per tile: the unit of every hand-off
+constexpr int kTilePages = kTile / kPage; // 4
 
-constexpr int kStages = 12;    // page stages in shared memory
-constexpr int kAStages = 4;    // TMEM A (key tile) stages
-constexpr int kDStages = 3;    // TMEM accumulator stages (128 fp32 columns each)
+constexpr int kStages = 16;    // page stages in shared memory
+constexpr int kAhead = 2;      // own tiles a worker group keeps loaded ahead of its epilogue
+constexpr int kAStages = 4;    // TMEM A (key tile) stages: kAhead per worker group
+constexpr int kDStages = 2;    // TMEM accumulator stages
 constexpr int kRing = 4;       // page-walker ring slots of 32 pages
-constexpr int kCap = 4096;     // candidate buffer of one segment (keys)
-constexpr int kKeyRing = 16;   // tiles of ranking keys between the workers and the selector
+constexpr int kCap = 2048;     // candidate buffer of one segment (keys)
+constexpr int kKeyRing = 8;    // tiles of ranking keys between the workers and the selector
 
 constexpr int kThreads = 512;
 // warp roles
@@ -73,16 +77,20 @@ constexpr int kBarSelect = 1;
 constexpr int kQEmptyCount = 1 + 4 * kWorkerGroups;  // MMA commit + every worker warp
 
 constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t a_col(int s) { return static_cast<uint32_t>(s) * 32u; }
-__host__ __device__ constexpr uint32_t d_col(int s) { return 128u + static_cast<uint32_t>(s) * 128u; }
+// A stage: kSub x 32 columns (128 lanes x 128 e4m3 bytes per sub-tile);
+// D stage: kSub x 64 fp32 columns (128 records x 64 heads per sub-tile).
+__host__ __device__ constexpr uint32_t a_col(int s) { return static_cast<uint32_t>(s) * 32u * kSub; }
+__host__ __device__ constexpr uint32_t d_col(int s) {
+  return 32u * kSub * kAStages + static_cast<uint32_t>(s) * 64u * kSub;
+}
 static_assert(d_col(kDStages) <= kTmemCols, "TMEM column map");
-static_assert(a_col(kAStages) <= d_col(0), "TMEM column map");
-static_assert(kAStages == 2 * kWorkerGroups, "each worker group loads two own tiles ahead");
+static_assert(kAStages == kAhead * kWorkerGroups, "each worker group owns kAhead key stages");
+static_assert(kStages % 4 == 0 && kCap >= CSA_MAX_K + kTile, "stage and buffer sizes");
 
-// B = the query's two e4m3 terms stacked as 128 rows (hi: heads 0-63, lo: heads
-// 0-63 again), so one N = 128 MMA yields both partial dots of every head; an
-// N = 128 MMA with A in TMEM costs the same issue time as N = 64.
-constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
+// One MMA: 128 records x 64 heads x 32 bytes of K. A sub-tile takes 8 of them:
+// the query's hi term over K = 0..127, then its lo term over the same K, all
+// into one accumulator, so each head's column holds k . (q * 2^e_h) directly.
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 64);
 constexpr uint32_t kNaNBits = 0x7FC00000u;
 
 struct Params {
@@ -154,14 +162,14 @@ __device__ __forceinline__ int32_t resident_count(const Params& P, int32_t req, 
   return n;
 }
 
-// Tiles of 128 records (two page slots) that row b covers.
+// Tiles (kTilePages page slots each) that row b covers.
 __device__ __forceinline__ int64_t query_tiles(const Params& P, int32_t b, int32_t* flags) {
   const int32_t req = row_request(P, b);
   if (req < 0) {
     *flags |= CSA_DEV_BAD_REQUEST;
     return 0;
   }
-  if (P.resident) return (resident_count(P, req, flags) + 1) / 2;
+  if (P.resident) return (resident_count(P, req, flags) + kTilePages - 1) / kTilePages;
   return (row_length(P, b, flags) + kTile - 1) / kTile;
 }
 
@@ -185,15 +193,15 @@ __host__ __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t total, int
   return c < grid - 1 ? c : grid - 1;
 }
 
-// Visible rows, logical page and physical page of page slot `half` of tile
+// Visible rows, logical page and physical page of page slot `j` (0..3) of tile
 // `lt` of row b. nrows = 0 marks a slot with nothing to score.
-__device__ PageInfo page_of(const Params& P, int32_t b, int64_t lt, int half, int32_t* flags) {
+__device__ PageInfo page_of(const Params& P, int32_t b, int64_t lt, int j, int32_t* flags) {
   PageInfo e{0, 0, 0, 0};
   const int32_t req = row_request(P, b);
   if (req < 0) return e;
   const int64_t L = row_length(P, b, flags);
   const int64_t npages = (L + kPage - 1) / kPage;
-  const int64_t slot = 2 * lt + half;
+  const int64_t slot = kTilePages * lt + j;
   int64_t p;
   if (P.resident) {
     if (slot >= resident_count(P, req, flags)) return e;
@@ -346,9 +354,12 @@ struct Cursor {
   }
 };
 
+// Broadcast of lane 0's value to the warp.
+__device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0; }
+
 __device__ void role_walker(const Params& P, Smem& S) {
   const int lane = threadIdx.x & 31;
-  const int64_t npg = 2 * S.plan.ntiles;
+  const int64_t npg = kTilePages * S.plan.ntiles;
   Cursor cur;
   cur.init(P, S.plan);
   int32_t flags = 0;
@@ -359,53 +370,73 @@ __device__ void role_walker(const Params& P, Smem& S) {
     if (lane == 0) ok = mbar_wait(smem_u32(&S.rempty[slot]), static_cast<uint32_t>(((batch / kRing) & 1) ^ 1),
                                   &S.abort_flag);
     if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-    // lane j handles page pg + j: tile offset j / 2, slot j % 2
+    // lane j handles page pg + j: tile offset j / 4, slot j % 4
     int32_t bb = cur.b;
-    int64_t ll = cur.lt + (lane >> 1), tb = cur.tiles;
+    int64_t ll = cur.lt + lane / kTilePages, tb = cur.tiles;
     while (bb < P.num_q && ll >= tb) {
       ll -= tb;
       bb = next_nonempty(P, bb + 1);
       tb = bb < P.num_q ? query_tiles(P, bb) : 0;
     }
     PageInfo e{0, -1, 0, 0};
-    if (pg + lane < npg && bb < P.num_q) e = page_of(P, bb, ll, lane & 1, &flags);
+    if (pg + lane < npg && bb < P.num_q) e = page_of(P, bb, ll, lane % kTilePages, &flags);
     S.ring[slot * 32 + lane] = e;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.rfull[slot]));
-    // the cursor moves on by 16 tiles
-    for (int t = 0; t < 16; ++t) cur.advance(P);
+    // the cursor moves on by 32 pages
+    for (int t = 0; t < 32 / kTilePages; ++t) cur.advance(P);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
   if (lane == 0 && flags) atomicOr(&S.status, flags);
 }
 
+// Page copies are issued by kIssueLanes lanes in lockstep, one page each: the
+// per-copy instruction latencies (ring read, barrier wait, expect_tx, copy) are
+// paid once per group instead of once per page.
+constexpr int kIssueLanes = 4;
+static_assert(kStages % kIssueLanes == 0 && 32 % kIssueLanes == 0, "issue groups");
+
 __device__ void role_issuer(const Params& P, Smem& S) {
-  const int64_t npg = 2 * S.plan.ntiles;
+  const int lane = threadIdx.x & 31;
+  const int64_t npg = kTilePages * S.plan.ntiles;
   const uint64_t policy = policy_evict_first();
-  int64_t pg = 0;
-  for (; pg < npg; ++pg) {
-    const int64_t batch = pg >> 5;
+  int64_t last = -1;  // last page this lane issued
+  for (int64_t pg0 = 0; pg0 < npg; pg0 += kIssueLanes) {
+    const int64_t batch = pg0 >> 5;
     const int slot = static_cast<int>(batch % kRing);
-    const int j = static_cast<int>(pg & 31);
-    if (j == 0 && !mbar_wait(smem_u32(&S.rfull[slot]), static_cast<uint32_t>((batch / kRing) & 1), &S.abort_flag))
-      break;
-    const PageInfo e = S.ring[slot * 32 + j];
-    const int s = static_cast<int>(pg % kStages);
-    if (!mbar_wait(smem_u32(&S.empty[s]), static_cast<uint32_t>(((pg / kStages) & 1) ^ 1), &S.abort_flag)) break;
-    S.info[s] = e;
-    const uint32_t fb = smem_u32(&S.full[s]);
-    if (e.nrows > 0) {
-      mbar_arrive_expect_tx(fb, kPageBytes);
-      bulk_g2s_hint(smem_u32(S.pages[s]), P.kv + static_cast<int64_t>(e.phys) * P.page_stride, kPageBytes, fb,
-                    policy);
-    } else {
-      mbar_arrive(fb);
+    const uint32_t rph = static_cast<uint32_t>((batch / kRing) & 1);
+    if ((pg0 & 31) == 0) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(smem_u32(&S.rfull[slot]), rph, &S.abort_flag);
+      if (!warp_ok(ok)) break;
     }
-    if (j == 31 || pg == npg - 1) mbar_arrive(smem_u32(&S.rempty[slot]));
+    const int64_t pg = pg0 + lane;
+    bool ok = true;
+    if (lane < kIssueLanes && pg < npg) {
+      mbar_wait_drain(smem_u32(&S.rfull[slot]), rph);  // complete: acquire the walker's entries
+      const PageInfo e = S.ring[slot * 32 + static_cast<int>(pg & 31)];
+      const int s = static_cast<int>(pg % kStages);
+      ok = mbar_wait(smem_u32(&S.empty[s]), static_cast<uint32_t>(((pg / kStages) & 1) ^ 1), &S.abort_flag);
+      if (ok) {
+        S.info[s] = e;
+        const uint32_t fb = smem_u32(&S.full[s]);
+        if (e.nrows > 0) {
+          mbar_arrive_expect_tx(fb, kPageBytes);
+          bulk_g2s_hint(smem_u32(S.pages[s]), P.kv + static_cast<int64_t>(e.phys) * P.page_stride, kPageBytes,
+                        fb, policy);
+        } else {
+          mbar_arrive(fb);
+        }
+        last = pg;
+      }
+    }
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    if (lane == 0 && (((pg0 + kIssueLanes) & 31) == 0 || pg0 + kIssueLanes >= npg))
+      mbar_arrive(smem_u32(&S.rempty[slot]));
   }
-  // Wait for every copy still in flight before the CTA may exit.
-  for (int64_t p = pg - 1; p >= 0 && p >= pg - kStages; --p)
+  // Wait for every copy this lane still has in flight before the CTA may exit.
+  for (int64_t p = last; p >= 0 && p > last - kStages; p -= kIssueLanes)
     mbar_wait_drain(smem_u32(&S.full[p % kStages]), static_cast<uint32_t>((p / kStages) & 1));
 }
 
@@ -426,11 +457,18 @@ __device__ void role_mma(const Params& P, Smem& S) {
     if (!mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((i / kDStages) & 1) ^ 1), &S.abort_flag))
       break;
     tc_fence_after();
-    const uint32_t dt = tmem + d_col(td);
-    const uint32_t at = tmem + a_col(ta);
-    const uint32_t bq = smem_u32(S.qbuf[qs][0]);  // 128 rows: [hi | lo]
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc, kk != 0);
+    for (int sub = 0; sub < kSub; ++sub) {
+      const uint32_t dt = tmem + d_col(td) + 64 * sub;
+      const uint32_t at = tmem + a_col(ta) + 32 * sub;
+#pragma unroll
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t bq = smem_u32(S.qbuf[qs][term]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc, (term | kk) != 0);
+      }
+    }
     mma_commit(smem_u32(&S.aempty[ta]));
     mma_commit(smem_u32(&S.dfull[td]));
     const bool seg_end = (i == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
@@ -522,61 +560,101 @@ __device__ void role_qprep(const Params& P, Smem& S) {
   if (lane == 0 && flags) atomicOr(&S.status, flags);
 }
 
-// Broadcast of lane 0's value to the warp.
-__device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0; }
-
 // One warp of a worker group: TMEM lane quarter q of every tile the group owns
 // (tiles i with i % kWorkerGroups == group). For each own tile it first moves
-// its 32 records' key bytes from the staged page into the TMEM A operand
-// ("load", two own tiles ahead of the epilogue) and later turns the MMA's head
-// dots into logits ("epilogue"). The warps never wait on each other.
+// its records' key bytes (32 rows of each of the kSub sub-tiles) from the
+// staged pages into the TMEM A operand ("load", kAhead own tiles ahead of the
+// epilogue) and later turns the MMA's head dots into logits ("epilogue"). The
+// warps never wait on each other.
 template <bool kTopk>
 __device__ void role_worker(const Params& P, Smem& S) {
   const int wi = (threadIdx.x >> 5) - kWarpWorker;
   const int group = wi >> 2;
   const int q = wi & 3;
   const int lane = threadIdx.x & 31;
-  const int half = q >> 1;                 // page of the tile this quarter reads
+  const int half = q >> 1;                 // page of each sub-tile this quarter reads
   const int r = 32 * (q & 1) + lane;       // record row inside that page
-  const int row = 32 * q + lane;           // record row inside the tile
+  const int row = 32 * q + lane;           // record row inside a sub-tile
   const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
   const uint32_t tmem = S.tmem_base;
   const int64_t nt = S.plan.ntiles;
 
-  // Loads own tile i. Returns false on abort; scale bits (NaN when the record
-  // is not visible) and the record's logical position come back in sc / pos.
-  auto load = [&](int64_t i, uint32_t& sc, uint32_t& pos) -> bool {
+  // Loads own tile i. Returns false on abort; per sub-tile, the scale bits (NaN
+  // when the record is not visible) and the record's logical position.
+  auto load = [&](int64_t i, uint32_t (&sc)[kSub], uint32_t (&pos)[kSub]) -> bool {
     const int ta = static_cast<int>(i % kAStages);
-    const int64_t pg = 2 * i + half;
-    const int s = static_cast<int>(pg % kStages);
-    const uint32_t ph = static_cast<uint32_t>((pg / kStages) & 1);
     bool ok = true;
-    if (lane == 0)
-      ok = mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag) &&
-           mbar_wait(smem_u32(&S.full[s]), ph, &S.abort_flag);
-    if (!warp_ok(ok)) return false;
-    mbar_wait_drain(smem_u32(&S.full[s]), ph);  // complete already: acquire for this lane
-    const PageInfo e = S.info[s];
-    const uint8_t* src = S.pages[s] + r * kRec;
-    uint32_t v[32];
+    if (lane == 0) {
+      ok = mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = *reinterpret_cast<const uint32_t*>(src + 4 * j);
-    const uint32_t scale = *reinterpret_cast<const uint32_t*>(src + kD);
-    sc = r < e.nrows ? scale : kNaNBits;
-    pos = static_cast<uint32_t>(e.lp * kPage + r);
-    tmem_st32(tmem + a_col(ta) + lane_off, v);
+      for (int sub = 0; sub < kSub; ++sub) {
+        const int64_t pg = kTilePages * i + 2 * sub + half;
+        ok = ok && mbar_wait(smem_u32(&S.full[pg % kStages]), static_cast<uint32_t>((pg / kStages) & 1),
+                             &S.abort_flag);
+      }
+    }
+    if (!warp_ok(ok)) return false;
+#pragma unroll
+    for (int sub = 0; sub < kSub; ++sub) {
+      const int64_t pg = kTilePages * i + 2 * sub + half;
+      const int s = static_cast<int>(pg % kStages);
+      mbar_wait_drain(smem_u32(&S.full[s]), static_cast<uint32_t>((pg / kStages) & 1));  // acquire
+      const PageInfo e = S.info[s];
+      const uint8_t* src = S.pages[s] + r * kRec;
+      uint32_t v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = *reinterpret_cast<const uint32_t*>(src + 4 * j);
+      const uint32_t scale = *reinterpret_cast<const uint32_t*>(src + kD);
+      sc[sub] = r < e.nrows ? scale : kNaNBits;
+      pos[sub] = static_cast<uint32_t>(e.lp * kPage + r);
+      tmem_st32(tmem + a_col(ta) + 32 * sub + lane_off, v);
+    }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(smem_u32(&S.empty[s]));
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub)
+        mbar_arrive(smem_u32(&S.empty[(kTilePages * i + 2 * sub + half) % kStages]));
       mbar_arrive(smem_u32(&S.afull[ta]));
     }
     return true;
   };
 
+  // Logit of this lane's record in sub-tile `sub` of D stage td.
+  auto logit_of = [&](int td, int sub, uint32_t sc, int seg) -> float {
+    const float s = __uint_as_float(sc);
+    const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
+    // relu(s * x) = |s| * relu(sign(s) * x); in practice every record of the warp
+    // has s >= 0 (one vote), and then the sign multiply drops out.
+    const float sg = s < 0.0f ? -1.0f : 1.0f;
+    const bool all_pos = __all_sync(0xFFFFFFFFu, sg > 0.0f);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kH; c += 16) {  // heads c .. c+15 of this lane's record
+      uint32_t x[16];
+      tmem_ld16(tmem + d_col(td) + 64 * sub + c + lane_off, x);
+      tmem_wait_ld();
+      float4 w4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w4[j] = wv[(c >> 2) + j];
+      const float* w = reinterpret_cast<const float*>(w4);
+      if (all_pos) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j & 7] = fmaf(fmaxf(__uint_as_float(x[j]), 0.f), w[j], acc[j & 7]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j & 7] = fmaf(fmaxf(sg * __uint_as_float(x[j]), 0.f), w[j], acc[j & 7]);
+      }
+    }
+    return fabsf(s) * (((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7])));
+  };
+
   // Epilogue of own tile i of row b, local tile lt, segment `seg`.
-  auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, uint32_t sc, uint32_t pos) -> bool {
+  auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, const uint32_t (&sc)[kSub],
+                      const uint32_t (&pos)[kSub]) -> bool {
     const int td = static_cast<int>(i % kDStages);
     const uint32_t dph = static_cast<uint32_t>((i / kDStages) & 1);
     bool ok = true;
@@ -584,66 +662,65 @@ __device__ void role_worker(const Params& P, Smem& S) {
     if (!warp_ok(ok)) return false;
     __syncwarp();
     tc_fence_after();
-    // columns 0-63: k . (q_hi * 2^e), 64-127: k . (q_lo * 2^e); a head's dot is their sum
-    const float s = __uint_as_float(sc);
-    const bool valid = !isnan(s);
-    const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    float logit[kSub];
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {  // heads 32*part .. 32*part + 31
-      uint32_t hi[32], lo[32];
-      tmem_ld32(tmem + d_col(td) + 32 * part + lane_off, hi);
-      tmem_ld32(tmem + d_col(td) + 64 + 32 * part + lane_off, lo);
-      tmem_wait_ld();
-      // relu(s * x) = s * max(x, 0) for s >= 0 and s * min(x, 0) for s < 0
-      if (s >= 0.0f) {
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 w = wv[8 * part + (h >> 2)];
-          a0 = fmaf(fmaxf(__uint_as_float(hi[h]) + __uint_as_float(lo[h]), 0.f), w.x, a0);
-          a1 = fmaf(fmaxf(__uint_as_float(hi[h + 1]) + __uint_as_float(lo[h + 1]), 0.f), w.y, a1);
-          a2 = fmaf(fmaxf(__uint_as_float(hi[h + 2]) + __uint_as_float(lo[h + 2]), 0.f), w.z, a2);
-          a3 = fmaf(fmaxf(__uint_as_float(hi[h + 3]) + __uint_as_float(lo[h + 3]), 0.f), w.w, a3);
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 w = wv[8 * part + (h >> 2)];
-          a0 = fmaf(fminf(__uint_as_float(hi[h]) + __uint_as_float(lo[h]), 0.f), w.x, a0);
-          a1 = fmaf(fminf(__uint_as_float(hi[h + 1]) + __uint_as_float(lo[h + 1]), 0.f), w.y, a1);
-          a2 = fmaf(fminf(__uint_as_float(hi[h + 2]) + __uint_as_float(lo[h + 2]), 0.f), w.z, a2);
-          a3 = fmaf(fminf(__uint_as_float(hi[h + 3]) + __uint_as_float(lo[h + 3]), 0.f), w.w, a3);
-        }
-      }
-    }
+    for (int sub = 0; sub < kSub; ++sub) logit[sub] = logit_of(td, sub, sc[sub], seg);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
-    const float logit = s * ((a0 + a1) + (a2 + a3));
 
     if constexpr (!kTopk) {
-      if (valid) P.scores[static_cast<int64_t>(b) * P.score_stride + lt * kTile + row] = 1.0f / (1.0f + expf(-logit));
+      float* out = P.scores + static_cast<int64_t>(b) * P.score_stride + lt * kTile + row;
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub)
+        if (!isnan(__uint_as_float(sc[sub]))) out[kMmaRows * sub] = __frcp_rn(1.0f + __expf(-logit[sub]));
     } else {
-      const uint64_t key = (valid && !isnan(logit)) ? make_key(logit, static_cast<int32_t>(pos)) : 0ull;
       const int slot = static_cast<int>(i % kKeyRing);
       bool ok2 = true;
       if (lane == 0)
         ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
                         &S.abort_flag);
       if (!warp_ok(ok2)) return false;
-      S.keys[slot][row] = key;
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {
+        const bool valid = !isnan(__uint_as_float(sc[sub])) && !isnan(logit[sub]);
+        S.keys[slot][kMmaRows * sub + row] = valid ? make_key(logit[sub], static_cast<int32_t>(pos[sub])) : 0ull;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.kfull[slot]));
     }
     return true;
   };
 
-  // scale bits and positions of the two own tiles loaded ahead (even / odd own tile)
-  uint32_t sc0 = 0, pos0 = 0, sc1 = 0, pos1 = 0;
+  // scale bits and positions of the own tiles loaded ahead, by own tile % kAhead
+  uint32_t scq[kAhead][kSub], posq[kAhead][kSub];
+#pragma unroll
+  for (int j = 0; j < kAhead; ++j)
+#pragma unroll
+    for (int u = 0; u < kSub; ++u) scq[j][u] = posq[j][u] = 0;
   bool ok = true;
-  // prologue: the group's first two tiles
-  if (group < nt) ok = load(group, sc0, pos0);
-  if (ok && group + kWorkerGroups < nt) ok = load(group + kWorkerGroups, sc1, pos1);
+  int64_t next_load = group, loaded = 0;  // next own tile to load, own tiles loaded
+  // Loads own tiles up to `limit` (one call site keeps the code small).
+  auto load_upto = [&](int64_t limit) {
+#pragma unroll 1
+    while (ok && next_load < nt && next_load <= limit) {
+      uint32_t a[kSub], p[kSub];
+      ok = load(next_load, a, p);
+      const int q4 = static_cast<int>(loaded % kAhead);
+#pragma unroll
+      for (int j = 0; j < kAhead; ++j)
+        if (q4 == j) {
+#pragma unroll
+          for (int u = 0; u < kSub; ++u) {
+            scq[j][u] = a[u];
+            posq[j][u] = p[u];
+          }
+        }
+      next_load += kWorkerGroups;
+      ++loaded;
+    }
+  };
+  load_upto(group + (kAhead - 1) * kWorkerGroups);
 
   Cursor cur;
   cur.init(P, S.plan);
@@ -662,13 +739,24 @@ __device__ void role_worker(const Params& P, Smem& S) {
         mbar_wait_drain(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1));
         wseg = seg;
       }
-      if ((mine & 1) == 0) {
-        ok = epilogue(t, cur.b, cur.lt, seg, sc0, pos0);
-        if (ok && t + 2 * kWorkerGroups < nt) ok = load(t + 2 * kWorkerGroups, sc0, pos0);
-      } else {
-        ok = epilogue(t, cur.b, cur.lt, seg, sc1, pos1);
-        if (ok && t + 2 * kWorkerGroups < nt) ok = load(t + 2 * kWorkerGroups, sc1, pos1);
+      const int q4 = static_cast<int>(mine % kAhead);
+      uint32_t my_sc[kSub], my_pos[kSub];
+#pragma unroll
+      for (int u = 0; u < kSub; ++u) {
+        my_sc[u] = scq[0][u];
+        my_pos[u] = posq[0][u];
       }
+#pragma unroll
+      for (int j = 1; j < kAhead; ++j)
+        if (q4 == j) {
+#pragma unroll
+          for (int u = 0; u < kSub; ++u) {
+            my_sc[u] = scq[j][u];
+            my_pos[u] = posq[j][u];
+          }
+        }
+      ok = epilogue(t, cur.b, cur.lt, seg, my_sc, my_pos);
+      load_upto(t + kAhead * kWorkerGroups);
       ++mine;
     }
     if (seg_end) {  // done with this segment's head weights
@@ -694,11 +782,15 @@ __device__ void role_select(const Params& P, Smem& S) {
     named_bar_sync(kBarSelect, 128);
     if (!S.go[t & 1]) break;
     mbar_wait_drain(smem_u32(&S.kfull[slot]), ph);
-    const uint64_t key = S.keys[slot][g];
-    append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+    const uint64_t tau = S.sel.tau;
+#pragma unroll
+    for (int j = 0; j < kTile; j += 128) {
+      const uint64_t key = S.keys[slot][j + g];
+      append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
+    }
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
-    shrink_if_above<128>(S.cand, S.scratch, kCap - 128, P.k, &S.sel, kBarSelect, g);
+    shrink_if_above<128>(S.cand, S.scratch, kCap - kTile, P.k, &S.sel, kBarSelect, g);
     const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
     if (seg_end) {
       shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, &S.sel, kBarSelect, g);
@@ -774,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
   tc_fence_after();
 
   if (warp == kWarpIssuer) {
-    if ((tid & 31) == 0) role_issuer(P, S);
+    role_issuer(P, S);
   } else if (warp == kWarpMma) {
     if ((tid & 31) == 0) role_mma(P, S);
   } else if (warp == kWarpWalker) {
@@ -865,7 +957,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
 // ------------------------------------------------------------------ unfused top-k
 
 constexpr int kTopkThreads = 128;
-constexpr int kTopkBatch = 8;
+constexpr int kTopkBatch = 4;
 constexpr int kTopkCtasPerSm = 4;
 
 struct TopkSmem {
@@ -896,32 +988,43 @@ __global__ void __launch_bounds__(kTopkThreads) topk_scores_kernel(const Params 
   cur.init(P, S.plan);
   for (int64_t i0 = 0; i0 < S.plan.ntiles; i0 += kTopkBatch) {
     const int nb = static_cast<int>(S.plan.ntiles - i0 < kTopkBatch ? S.plan.ntiles - i0 : kTopkBatch);
-    float val[kTopkBatch];
-    int32_t pos[kTopkBatch];
-    bool ok[kTopkBatch];
+    // this thread's columns of the next nb tiles: tid and tid + 128 of each
+    float val[kTopkBatch][2];
+    int32_t pos[kTopkBatch][2];
+    bool ok[kTopkBatch][2];
     Cursor c = cur;
 #pragma unroll
     for (int u = 0; u < kTopkBatch; ++u) {
-      ok[u] = false;
-      pos[u] = 0;
-      val[u] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        ok[u][h] = false;
+        pos[u][h] = 0;
+        val[u][h] = 0.f;
+      }
       if (u < nb) {
-        const int64_t col = c.lt * kTile + tid;
-        const PageInfo e = page_of(P, c.b, c.lt, tid >> 6, &flags);
-        const int r = tid & 63;
-        if (r < e.nrows) {
-          ok[u] = true;
-          pos[u] = e.lp * kPage + r;
-          val[u] = P.in_scores[static_cast<int64_t>(c.b) * P.score_stride + col];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int colt = 128 * h + tid;  // column inside the tile
+          const PageInfo e = page_of(P, c.b, c.lt, colt >> 6, &flags);
+          const int r = colt & 63;
+          if (r < e.nrows) {
+            ok[u][h] = true;
+            pos[u][h] = e.lp * kPage + r;
+            val[u][h] = P.in_scores[static_cast<int64_t>(c.b) * P.score_stride + c.lt * kTile + colt];
+          }
         }
         c.advance(P);
       }
     }
     for (int u = 0; u < nb; ++u) {
-      const uint64_t key = (ok[u] && !isnan(val[u])) ? make_key(val[u], pos[u]) : 0ull;
-      append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+      const uint64_t tau = S.sel.tau;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t key = (ok[u][h] && !isnan(val[u][h])) ? make_key(val[u][h], pos[u][h]) : 0ull;
+        append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
+      }
       __syncthreads();
-      shrink_if_above<kTopkThreads>(S.cand, S.scratch, kCap - kTopkThreads, P.k, &S.sel, 0, tid);
+      shrink_if_above<kTopkThreads>(S.cand, S.scratch, kCap - kTile, P.k, &S.sel, 0, tid);
       const bool seg_end = (i0 + u == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
       if (seg_end) {
         shrink_if_above<kTopkThreads>(S.cand, S.scratch, P.k, P.k, &S.sel, 0, tid);

@@ -65,18 +65,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // raises the CTA's abort flag and reports a timeout instead of hanging.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
-// Waits for the phase of `bar` with parity `parity` to complete. Returns false
-// when the CTA-wide abort flag is raised or the time limit passes (the flag is
-// then raised here). Polls the flag and the clock every 64 failed probes.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
+// Probes between two looks at the clock in the bounded waits: a wait that
+// completes within the first probes never reads %globaltimer.
+constexpr uint32_t kProbesPerClockCheck = 256;
+
+// Slow path of mbar_wait, kept out of line so that the many call sites stay
+// small (the persistent kernels are sensitive to instruction-cache pressure):
+// polls until the phase completes, the CTA-wide abort flag is raised, or the
+// time limit passes (the flag is then raised here).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  uint64_t t0 = 0;
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
+    if (++spins % kProbesPerClockCheck == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
         *abort_flag = 1;
         return false;
       }
@@ -84,14 +91,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Same wait, ignoring the abort flag: used while draining copies in flight
-// before the CTA exits. Still bounded by the time limit.
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  uint64_t t0 = globaltimer_ns();
+// Waits for the phase of `bar` with parity `parity` to complete. Returns false
+// when the CTA-wide abort flag is raised or the time limit passes.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag);
+}
+
+__device__ __noinline__ bool mbar_wait_drain_slow(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (++spins % kProbesPerClockCheck == 0) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        return false;
+      }
+    }
   }
   return true;
+}
+
+// Same wait, ignoring the abort flag: used to acquire a phase that another lane
+// has already seen complete, and while draining copies in flight before the CTA
+// exits. Still bounded by the time limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_drain_slow(bar, parity);
 }
 
 // ----------------------------------------------------------------- bulk copy
@@ -211,6 +239,17 @@ __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b)
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& a, uint32_t& b) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr)
                : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: thread t reads lane (base + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
 }
 
 // 32 lanes x 32 bits, 32 consecutive columns: thread t reads lane (base + t).
