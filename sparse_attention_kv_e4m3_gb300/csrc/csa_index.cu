@@ -60,9 +60,8 @@ constexpr int kTile = kSub * kMmaRows;    // records per tile: the unit of every
 constexpr int kTilePages = kTile / kPage; // 4
 
 constexpr int kStages = 16;    // page stages in shared memory
-constexpr int kAhead = 2;      // own tiles a worker group keeps loaded ahead of its epilogue
-constexpr int kAStages = 4;    // TMEM A (key tile) stages: kAhead per worker group
-constexpr int kDStages = 2;    // TMEM accumulator stages
+constexpr int kAStages = 2;    // TMEM A (key tile) stages: one per worker group
+constexpr int kDStages = 3;    // TMEM accumulator stages
 constexpr int kRing = 4;       // page-walker ring slots of 32 pages
 constexpr int kCap = 2048;     // candidate buffer of one segment (keys)
 constexpr int kKeyRing = 8;    // tiles of ranking keys between the workers and the selector
@@ -84,7 +83,7 @@ __host__ __device__ constexpr uint32_t d_col(int s) {
   return 32u * kSub * kAStages + static_cast<uint32_t>(s) * 64u * kSub;
 }
 static_assert(d_col(kDStages) <= kTmemCols, "TMEM column map");
-static_assert(kAStages == kAhead * kWorkerGroups, "each worker group owns kAhead key stages");
+static_assert(kAStages == kWorkerGroups, "each worker group owns one key stage");
 static_assert(kStages % 4 == 0 && kCap >= CSA_MAX_K + kTile, "stage and buffer sizes");
 
 // One MMA: 128 records x 64 heads x 32 bytes of K. A sub-tile takes 8 of them:
@@ -561,11 +560,12 @@ __device__ void role_qprep(const Params& P, Smem& S) {
 }
 
 // One warp of a worker group: TMEM lane quarter q of every tile the group owns
-// (tiles i with i % kWorkerGroups == group). For each own tile it first moves
-// its records' key bytes (32 rows of each of the kSub sub-tiles) from the
-// staged pages into the TMEM A operand ("load", kAhead own tiles ahead of the
-// epilogue) and later turns the MMA's head dots into logits ("epilogue"). The
-// warps never wait on each other.
+// (tiles i with i % kWorkerGroups == group). It moves its records' key bytes
+// (32 rows of each of the kSub sub-tiles) from the staged pages into the TMEM
+// A operand ("load") and turns the MMA's head dots into logits ("epilogue").
+// Once the MMA of own tile t is done, the group's key stage is free: the warp
+// loads own tile t + kWorkerGroups first, so that its MMA overlaps the
+// epilogue of t. The warps never wait on each other.
 template <bool kTopk>
 __device__ void role_worker(const Params& P, Smem& S) {
   const int wi = (threadIdx.x >> 5) - kWarpWorker;
@@ -652,15 +652,11 @@ __device__ void role_worker(const Params& P, Smem& S) {
     return fabsf(s) * (((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7])));
   };
 
-  // Epilogue of own tile i of row b, local tile lt, segment `seg`.
+  // Epilogue of own tile i of row b, local tile lt, segment `seg`; the caller
+  // has seen the tile's accumulator complete.
   auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, const uint32_t (&sc)[kSub],
                       const uint32_t (&pos)[kSub]) -> bool {
     const int td = static_cast<int>(i % kDStages);
-    const uint32_t dph = static_cast<uint32_t>((i / kDStages) & 1);
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait(smem_u32(&S.dfull[td]), dph, &S.abort_flag);
-    if (!warp_ok(ok)) return false;
-    __syncwarp();
     tc_fence_after();
     float logit[kSub];
 #pragma unroll
@@ -692,40 +688,16 @@ __device__ void role_worker(const Params& P, Smem& S) {
     return true;
   };
 
-  // scale bits and positions of the own tiles loaded ahead, by own tile % kAhead
-  uint32_t scq[kAhead][kSub], posq[kAhead][kSub];
+  // scale bits and positions of the current own tile and of the next one
+  uint32_t cur_sc[kSub], cur_pos[kSub], nxt_sc[kSub], nxt_pos[kSub];
 #pragma unroll
-  for (int j = 0; j < kAhead; ++j)
-#pragma unroll
-    for (int u = 0; u < kSub; ++u) scq[j][u] = posq[j][u] = 0;
+  for (int u = 0; u < kSub; ++u) cur_sc[u] = cur_pos[u] = nxt_sc[u] = nxt_pos[u] = 0;
   bool ok = true;
-  int64_t next_load = group, loaded = 0;  // next own tile to load, own tiles loaded
-  // Loads own tiles up to `limit` (one call site keeps the code small).
-  auto load_upto = [&](int64_t limit) {
-#pragma unroll 1
-    while (ok && next_load < nt && next_load <= limit) {
-      uint32_t a[kSub], p[kSub];
-      ok = load(next_load, a, p);
-      const int q4 = static_cast<int>(loaded % kAhead);
-#pragma unroll
-      for (int j = 0; j < kAhead; ++j)
-        if (q4 == j) {
-#pragma unroll
-          for (int u = 0; u < kSub; ++u) {
-            scq[j][u] = a[u];
-            posq[j][u] = p[u];
-          }
-        }
-      next_load += kWorkerGroups;
-      ++loaded;
-    }
-  };
-  load_upto(group + (kAhead - 1) * kWorkerGroups);
+  if (group < nt) ok = load(group, cur_sc, cur_pos);
 
   Cursor cur;
   cur.init(P, S.plan);
   int seg = 0, wseg = -1;
-  int64_t mine = 0;  // own tiles finished
   for (int64_t t = 0; ok && t < nt; ++t) {
     const bool seg_start = (t == 0) || (cur.lt == 0);
     if (seg_start && t > 0) ++seg;
@@ -739,25 +711,22 @@ __device__ void role_worker(const Params& P, Smem& S) {
         mbar_wait_drain(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1));
         wseg = seg;
       }
-      const int q4 = static_cast<int>(mine % kAhead);
-      uint32_t my_sc[kSub], my_pos[kSub];
+      // MMA of tile t done: its accumulator is ready and the group's key stage is free
+      bool okd = true;
+      if (lane == 0)
+        okd = mbar_wait(smem_u32(&S.dfull[t % kDStages]), static_cast<uint32_t>((t / kDStages) & 1),
+                        &S.abort_flag);
+      if (!warp_ok(okd)) break;
+      if (t + kWorkerGroups < nt) {
+        ok = load(t + kWorkerGroups, nxt_sc, nxt_pos);
+        if (!ok) break;
+      }
+      ok = epilogue(t, cur.b, cur.lt, seg, cur_sc, cur_pos);
 #pragma unroll
       for (int u = 0; u < kSub; ++u) {
-        my_sc[u] = scq[0][u];
-        my_pos[u] = posq[0][u];
+        cur_sc[u] = nxt_sc[u];
+        cur_pos[u] = nxt_pos[u];
       }
-#pragma unroll
-      for (int j = 1; j < kAhead; ++j)
-        if (q4 == j) {
-#pragma unroll
-          for (int u = 0; u < kSub; ++u) {
-            my_sc[u] = scq[j][u];
-            my_pos[u] = posq[j][u];
-          }
-        }
-      ok = epilogue(t, cur.b, cur.lt, seg, my_sc, my_pos);
-      load_upto(t + kAhead * kWorkerGroups);
-      ++mine;
     }
     if (seg_end) {  // done with this segment's head weights
       __syncwarp();
