@@ -92,6 +92,11 @@ static_assert(kStages % 4 == 0 && kCap >= CSA_MAX_K + kTile, "stage and buffer s
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 64);
 constexpr uint32_t kNaNBits = 0x7FC00000u;
 
+// Keys kept by an intermediate cut of a candidate buffer: at least k, at most
+// half as many again (or the scratch size), so that a cheap, inexact radix
+// select (usually two digit passes) suffices until a segment's final cut.
+__device__ __forceinline__ int loose_keep(int k) { return min(CSA_MAX_K, k + (k >> 1)); }
+
 struct Params {
   const uint16_t* q;
   const float* w;
@@ -759,10 +764,10 @@ __device__ void role_select(const Params& P, Smem& S) {
     }
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
-    shrink_if_above<128>(S.cand, S.scratch, kCap - kTile, P.k, &S.sel, kBarSelect, g);
+    shrink_if_above<128>(S.cand, S.scratch, kCap - kTile, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
     const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
     if (seg_end) {
-      shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, &S.sel, kBarSelect, g);
+      shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, P.k, &S.sel, kBarSelect, g);
       const int n = static_cast<int>(S.sel.n);
       uint8_t* out = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
       uint64_t* ent = reinterpret_cast<uint64_t*>(out + 16);
@@ -862,17 +867,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
 
 // ------------------------------------------------------------------ merge
 
-constexpr int kMergeThreads = 256;
-constexpr int kMergeCap = 8192;
+constexpr int kMergeThreads = 512;
+constexpr int kMergeCap = 8192;   // candidate buffer of the general path
+constexpr int kMergeSort = 2048;  // rows with at most this many candidates are sorted whole
+constexpr int kMergeSlots = CSA_MAX_CTAS + 1;
 
 struct MergeSmem {
   uint64_t cand[kMergeCap];
   uint64_t scratch[CSA_MAX_K];
+  int32_t offs[kMergeSlots];  // exclusive prefix of the row's slot counts
   SelectShared sel;
 };
 
 // One CTA per query row: gathers the row's segment slots, keeps the exact top
 // k and writes them sorted by (value desc, position asc), padded with -1 / 0.
+// Rows with at most kMergeSort candidates (the usual case: a few slots of at
+// most k keys) are sorted whole; larger ones go through the thresholded buffer.
 template <bool kFromLogit>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, int32_t* idx, float* vals) {
   extern __shared__ uint8_t smem_raw[];
@@ -884,34 +894,75 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
     S.sel.n = 0;
     S.sel.tau = 0;
   }
-  __syncthreads();
   const int64_t t0 = tile_off[b], t1 = tile_off[b + 1], total = tile_off[P.num_q];
+  int64_t c0 = 0, c1 = -1;
   if (t0 < t1) {
-    const int64_t c0 = cta_of(t0, total, P.grid), c1 = cta_of(t1 - 1, total, P.grid);
-    for (int64_t c = c0; c <= c1; ++c) {
-      if (cta_begin(c, total, P.grid) == cta_begin(c + 1, total, P.grid)) continue;
-      const uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(b) + c) * P.slot_bytes;
-      int cnt = *reinterpret_cast<const int32_t*>(slot);
-      cnt = cnt < 0 ? 0 : (cnt > P.k ? P.k : cnt);  // a slot never holds more than k keys
-      const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot + 16);
+    c0 = cta_of(t0, total, P.grid);
+    c1 = cta_of(t1 - 1, total, P.grid);
+  }
+  const int nslots = static_cast<int>(c1 - c0 + 1);  // 0 for an empty row
+  auto slot_ptr = [&](int j) {
+    return P.ws + P.slots_offset + (static_cast<int64_t>(b) + c0 + j) * P.slot_bytes;
+  };
+  // slot counts (0 for CTAs with an empty range) and their prefix, by warp 0
+  if (tid < 32) {
+    int run = 0;
+    for (int base = 0; base < nslots; base += 32) {
+      const int j = base + tid;
+      int cnt = 0;
+      if (j < nslots) {
+        const int64_t c = c0 + j;
+        if (cta_begin(c, total, P.grid) != cta_begin(c + 1, total, P.grid)) {
+          cnt = *reinterpret_cast<const int32_t*>(slot_ptr(j));
+          cnt = cnt < 0 ? 0 : (cnt > P.k ? P.k : cnt);  // a slot never holds more than k keys
+        }
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (tid >= o) incl += v;
+      }
+      if (j < nslots) S.offs[j] = run + incl - cnt;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (tid == 0) S.offs[nslots] = run;
+  }
+  __syncthreads();
+  const int ntot = S.offs[nslots];
+  int n;
+  if (ntot <= kMergeSort) {
+    for (int j = 0; j < nslots; ++j) {
+      const int o = S.offs[j], cnt = S.offs[j + 1] - o;
+      const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot_ptr(j) + 16);
+      for (int i = tid; i < cnt; i += kMergeThreads) S.cand[o + i] = ent[i];
+    }
+    n = ntot;
+  } else {
+    for (int j = 0; j < nslots; ++j) {
+      const int cnt = S.offs[j + 1] - S.offs[j];
+      const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot_ptr(j) + 16);
       for (int base = 0; base < cnt; base += kMergeThreads) {
         const uint64_t key = (base + tid < cnt) ? ent[base + tid] : 0ull;
-        append_key(S.cand, key, key != 0ull && key > S.sel.tau, &S.sel);
+        const uint64_t tau = S.sel.tau;
+        append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
         __syncthreads();
-        shrink_if_above<kMergeThreads>(S.cand, S.scratch, kMergeCap - kMergeThreads, P.k, &S.sel, 0, tid);
+        shrink_if_above<kMergeThreads>(S.cand, S.scratch, kMergeCap - kMergeThreads, P.k, loose_keep(P.k), &S.sel,
+                                       0, tid);
       }
     }
+    shrink_if_above<kMergeThreads>(S.cand, S.scratch, P.k, P.k, P.k, &S.sel, 0, tid);
+    n = static_cast<int>(S.sel.n);
   }
-  shrink_if_above<kMergeThreads>(S.cand, S.scratch, P.k, P.k, &S.sel, 0, tid);
-  const int n = static_cast<int>(S.sel.n);
   int m = 1;
   while (m < n) m <<= 1;
   for (int j = n + tid; j < m; j += kMergeThreads) S.cand[j] = 0ull;
   __syncthreads();
   if (m > 1) bitonic_sort_desc<kMergeThreads>(S.cand, m, 0, tid);
+  const int kept = n < P.k ? n : P.k;
   for (int j = tid; j < P.k; j += kMergeThreads) {
     const int64_t o = static_cast<int64_t>(b) * P.k + j;
-    if (j < n) {
+    if (j < kept) {
       const uint64_t key = S.cand[j];
       const float v = key_value(key);
       idx[o] = key_position(key);
@@ -993,10 +1044,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_scores_kernel(const Params 
         append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
       }
       __syncthreads();
-      shrink_if_above<kTopkThreads>(S.cand, S.scratch, kCap - kTile, P.k, &S.sel, 0, tid);
+      shrink_if_above<kTopkThreads>(S.cand, S.scratch, kCap - kTile, P.k, loose_keep(P.k), &S.sel, 0, tid);
       const bool seg_end = (i0 + u == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
       if (seg_end) {
-        shrink_if_above<kTopkThreads>(S.cand, S.scratch, P.k, P.k, &S.sel, 0, tid);
+        shrink_if_above<kTopkThreads>(S.cand, S.scratch, P.k, P.k, P.k, &S.sel, 0, tid);
         const int n = static_cast<int>(S.sel.n);
         uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
         uint64_t* ent = reinterpret_cast<uint64_t*>(slot + 16);

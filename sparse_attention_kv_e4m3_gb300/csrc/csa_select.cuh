@@ -53,11 +53,15 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Returns T such that exactly `kk` of keys[0, n) are >= T (1 <= kk <= n, keys
-// distinct). MSB-first radix select with 8-bit digits; stops as soon as the
-// group sharing the current prefix is taken whole.
+// Returns T such that between `kk` and `max_keep` of keys[0, n) are >= T
+// (1 <= kk <= max_keep, kk <= n, keys distinct); with max_keep == kk, T is the
+// kk-th largest key. MSB-first radix select with 8-bit digits: after each digit,
+// the keys whose prefix is above the boundary digit are in, those below are out,
+// and it stops as soon as taking the boundary group whole keeps at most
+// max_keep keys.
 template <int NT>
-__device__ uint64_t select_kth(const uint64_t* keys, int n, int kk, SelectShared* ss, int bar, int gtid) {
+__device__ uint64_t select_kth(const uint64_t* keys, int n, int kk, int max_keep, SelectShared* ss, int bar,
+                               int gtid) {
   const int lane = gtid & 31;
   const int warp = gtid >> 5;
   uint64_t prefix = 0, mask = 0;
@@ -113,7 +117,8 @@ __device__ uint64_t select_kth(const uint64_t* keys, int n, int kk, SelectShared
     need -= above;
     prefix |= static_cast<uint64_t>(digit) << shift;
     mask |= static_cast<uint64_t>(0xFFu) << shift;
-    if (group == need) return prefix;  // every key >= prefix is in: exactly kk of them
+    // keys >= prefix: (kk - need) above the group, plus the group itself
+    if ((kk - need) + group <= max_keep) return prefix;
   }
   return prefix;
 }
@@ -150,15 +155,18 @@ __device__ __forceinline__ void append_key(uint64_t* buf, uint64_t key, bool tak
   if (take) buf[base + __popc(ballot & lanemask_lt())] = key;
 }
 
-// Cuts the buffer down to its kk best keys when it holds more than `limit`,
-// and raises the admission threshold to the new k-th key. Group-uniform.
+// Cuts the buffer down when it holds more than `limit` keys: to the keys >= T
+// for a T that keeps between kk and max_keep of them (exactly the kk best when
+// max_keep == kk), and raises the admission threshold to T. Any such T is a
+// valid threshold: at least kk keys seen so far are >= T, so no key below T can
+// be among the kk best. Group-uniform.
 template <int NT>
-__device__ void shrink_if_above(uint64_t* buf, uint64_t* scratch, int limit, int kk, SelectShared* ss, int bar,
-                                int gtid) {
+__device__ void shrink_if_above(uint64_t* buf, uint64_t* scratch, int limit, int kk, int max_keep, SelectShared* ss,
+                                int bar, int gtid) {
   const int n = static_cast<int>(ss->n);
   if (n <= limit || n <= kk) return;
-  const uint64_t T = select_kth<NT>(buf, n, kk, ss, bar, gtid);
-  const int m = compact_ge<NT>(buf, n, T, scratch, kk, ss, bar, gtid);
+  const uint64_t T = select_kth<NT>(buf, n, kk, max_keep, ss, bar, gtid);
+  const int m = compact_ge<NT>(buf, n, T, scratch, max_keep, ss, bar, gtid);
   if (gtid == 0) {
     ss->n = static_cast<uint32_t>(m);
     ss->tau = T ? T - 1 : 0;  // admit keys > T - 1, i.e. >= T; later keys are new (distinct)
