@@ -207,8 +207,8 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
  * array that every GPU loading the library holds until the process exits.
  *
  * Limit: the call needs 256-byte-rounded 4*(num_q+1) bytes plus
- * (num_q + number of SMs) * (16 + 8*k rounded up to 16) bytes of that array
- * (64 rows at k = 512 on a 152-SM GB300 use about 0.9 MB); larger requests return
+ * (num_q + number of SMs) * (16 + 8*min(1024, k + k/2) rounded up to 16) bytes of
+ * that array (64 rows at k = 512 on a 152-SM GB300 use about 1.3 MB); larger requests return
  * CSA_ERR_WORKSPACE before anything is launched.
  *
  * The first call on a device looks up the array's device address for that

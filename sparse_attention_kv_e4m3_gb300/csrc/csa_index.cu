@@ -39,6 +39,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -92,10 +93,22 @@ static_assert(kStages % 4 == 0 && kCap >= CSA_MAX_K + kTile, "stage and buffer s
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 64);
 constexpr uint32_t kNaNBits = 0x7FC00000u;
 
-// Keys kept by an intermediate cut of a candidate buffer: at least k, at most
-// half as many again (or the scratch size), so that a cheap, inexact radix
-// select (usually two digit passes) suffices until a segment's final cut.
-__device__ __forceinline__ int loose_keep(int k) { return min(CSA_MAX_K, k + (k >> 1)); }
+// Keys kept by a cut of a candidate buffer: at least k, at most half as many
+// again (or the scratch size). The window is wide enough for a sampled
+// threshold to land in it almost always; a segment's slot holds this many keys
+// at most, unsorted, and only the merge finds the exact k best.
+__host__ __device__ __forceinline__ int loose_keep(int k) {
+  const int m = k + (k >> 1);
+  return m < CSA_MAX_K ? m : CSA_MAX_K;
+}
+
+// Keys the merge sorts: the power of two at or above 2k (at least 64, at most
+// CSA_MAX_K); a row with more candidates is first cut to between k and this.
+__host__ __device__ __forceinline__ int merge_window(int k) {
+  int w = 64;
+  while (w < 2 * k) w <<= 1;
+  return w < CSA_MAX_K ? w : CSA_MAX_K;
+}
 
 struct Params {
   const uint16_t* q;
@@ -311,8 +324,10 @@ struct __align__(1024) Smem {
   uint8_t pages[kStages][kPageBytes];
   uint64_t cand[kCap];
   uint64_t scratch[CSA_MAX_K];
-  uint64_t keys[kKeyRing][kTile];  // ranking keys of one tile, worker -> selector
-  float wbuf[2][kH];
+  uint64_t keys[kKeyRing][kTile];  // a tile's admissible keys, worker -> selector: 64 per worker warp
+  uint32_t kcnt[kKeyRing][4];      // keys in each worker warp's region of the slot
+  uint64_t filt;                   // (segment << 32) | value word of the selector's current threshold
+  alignas(16) float wbuf[2][kH];   // read as float4
   PageInfo ring[kRing * 32];
   PageInfo info[kStages];
   uint64_t full[kStages], empty[kStages];
@@ -330,6 +345,20 @@ struct __align__(1024) Smem {
   int32_t status;
   int32_t go[2];                   // selector leader's wait result, by tile parity
 };
+// alignment each field's accesses need: swizzle atoms, bulk-copy destinations, float4 loads
+static_assert(offsetof(Smem, qbuf) % 1024 == 0, "128-byte swizzle atoms need 1024-byte alignment");
+static_assert(offsetof(Smem, pages) % 16 == 0 && kPageBytes % 16 == 0, "bulk copies land on 16-byte boundaries");
+static_assert(offsetof(Smem, wbuf) % 16 == 0, "head weights are read as float4");
+static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, filt) % 8 == 0, "mbarriers and 64-bit words");
+
+// The worker-side filter of segment `seg`: a key whose value word is below the
+// returned word cannot reach the segment's best k (the selector has already
+// seen k keys at or above it); 0 admits every key. A word tagged with another
+// segment is stale and admits everything.
+__device__ __forceinline__ uint32_t filter_word(const Smem& S, int seg) {
+  const uint64_t f = *reinterpret_cast<const volatile uint64_t*>(&S.filt);
+  return static_cast<uint32_t>(f >> 32) == static_cast<uint32_t>(seg) ? static_cast<uint32_t>(f) : 0u;
+}
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -360,6 +389,7 @@ struct Cursor {
 
 // Broadcast of lane 0's value to the warp.
 __device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0; }
+
 
 __device__ void role_walker(const Params& P, Smem& S) {
   const int lane = threadIdx.x & 31;
@@ -627,6 +657,7 @@ __device__ void role_worker(const Params& P, Smem& S) {
   };
 
   // Logit of this lane's record in sub-tile `sub` of D stage td.
+  // Logit of this lane's record in sub-tile `sub` of D stage td.
   auto logit_of = [&](int td, int sub, uint32_t sc, int seg) -> float {
     const float s = __uint_as_float(sc);
     const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
@@ -682,11 +713,21 @@ __device__ void role_worker(const Params& P, Smem& S) {
         ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
                         &S.abort_flag);
       if (!warp_ok(ok2)) return false;
+      // keys that can still make the segment's best k, packed into this warp's region
+      const uint32_t thr = filter_word(S, seg);
+      const uint32_t lt = lanemask_lt();
+      uint64_t* region = S.keys[slot] + 64 * q;
+      uint32_t cnt = 0;
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub) {
         const bool valid = !isnan(__uint_as_float(sc[sub])) && !isnan(logit[sub]);
-        S.keys[slot][kMmaRows * sub + row] = valid ? make_key(logit[sub], static_cast<int32_t>(pos[sub])) : 0ull;
+        const uint64_t key = valid ? make_key(logit[sub], static_cast<int32_t>(pos[sub])) : 0ull;
+        const bool take = valid && static_cast<uint32_t>(key >> 32) >= thr;
+        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, take);
+        if (take) region[cnt + __popc(ballot & lt)] = key;
+        cnt += __popc(ballot);
       }
+      if (lane == 0) S.kcnt[slot][q] = cnt;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.kfull[slot]));
     }
@@ -741,33 +782,36 @@ __device__ void role_worker(const Params& P, Smem& S) {
   }
 }
 
-// Top-k selector (warps 12-15): takes every tile's 128 keys in tile order,
-// keeps those above the segment's running threshold in a shared-memory
-// buffer, cuts the buffer back to the best k when it fills, and writes each
-// segment's best k to workspace slot (row + CTA).
+// Top-k selector (warps 12-15): takes each tile's admissible keys in tile
+// order (the workers have dropped keys below the segment's published
+// threshold), keeps those above the running threshold in a shared-memory
+// buffer, cuts the buffer back to between k and loose_keep(k) keys when it
+// fills, publishes the new threshold to the workers, and writes each segment's
+// survivors (at most loose_keep(k), unsorted) to workspace slot (row + CTA).
 __device__ void role_select(const Params& P, Smem& S) {
   const int g = threadIdx.x - kWarpSelect * 32;
+  const int sw = g >> 5, lane = g & 31;
   Cursor cur;
   cur.init(P, S.plan);
+  int seg = 0;
   for (int64_t t = 0; t < S.plan.ntiles; ++t) {
     const int slot = static_cast<int>(t % kKeyRing);
     const uint32_t ph = static_cast<uint32_t>((t / kKeyRing) & 1);
     if (g == 0) S.go[t & 1] = mbar_wait(smem_u32(&S.kfull[slot]), ph, &S.abort_flag) ? 1 : 0;
-    named_bar_sync(kBarSelect, 128);
+    named_bar_sync(kBarSelect, 128);  // passes the leader's acquire of the slot on to the group
     if (!S.go[t & 1]) break;
-    mbar_wait_drain(smem_u32(&S.kfull[slot]), ph);
     const uint64_t tau = S.sel.tau;
-#pragma unroll
-    for (int j = 0; j < kTile; j += 128) {
-      const uint64_t key = S.keys[slot][j + g];
-      append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
-    }
+    const int c = static_cast<int>(S.kcnt[slot][sw]);
+    const uint64_t* region = S.keys[slot] + 64 * sw;
+    const uint64_t k0 = lane < c ? region[lane] : 0ull;
+    const uint64_t k1 = lane + 32 < c ? region[lane + 32] : 0ull;
+    append_keys2(S.cand, k0, k0 > tau, k1, k1 > tau, &S.sel);
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
-    shrink_if_above<128>(S.cand, S.scratch, kCap - kTile, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+    shrink_if_above<128, 128>(S.cand, S.scratch, kCap - kTile, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
     const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
     if (seg_end) {
-      shrink_if_above<128>(S.cand, S.scratch, P.k, P.k, P.k, &S.sel, kBarSelect, g);
+      shrink_if_above<128, 128>(S.cand, S.scratch, loose_keep(P.k), P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
       const int n = static_cast<int>(S.sel.n);
       uint8_t* out = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
       uint64_t* ent = reinterpret_cast<uint64_t*>(out + 16);
@@ -779,6 +823,12 @@ __device__ void role_select(const Params& P, Smem& S) {
         S.sel.tau = 0;
       }
       named_bar_sync(kBarSelect, 128);
+      ++seg;
+    }
+    if (g == 0) {
+      const uint64_t T = S.sel.tau + 1;  // keys >= T are admitted
+      *reinterpret_cast<volatile uint64_t*>(&S.filt) =
+          (static_cast<uint64_t>(static_cast<uint32_t>(seg)) << 32) | static_cast<uint32_t>(S.sel.tau ? T >> 32 : 0);
     }
     cur.advance(P);
   }
@@ -795,6 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
     S.status = 0;
     S.sel.n = 0;
     S.sel.tau = 0;
+    S.filt = ~0ull;  // tagged with no segment: admits everything
   }
   __syncthreads();
   make_plan<kThreads>(P, &S.plan, S.warp_sums,
@@ -869,7 +920,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
 
 constexpr int kMergeThreads = 512;
 constexpr int kMergeCap = 8192;   // candidate buffer of the general path
-constexpr int kMergeSort = 2048;  // rows with at most this many candidates are sorted whole
 constexpr int kMergeSlots = CSA_MAX_CTAS + 1;
 
 struct MergeSmem {
@@ -879,10 +929,11 @@ struct MergeSmem {
   SelectShared sel;
 };
 
-// One CTA per query row: gathers the row's segment slots, keeps the exact top
-// k and writes them sorted by (value desc, position asc), padded with -1 / 0.
-// Rows with at most kMergeSort candidates (the usual case: a few slots of at
-// most k keys) are sorted whole; larger ones go through the thresholded buffer.
+// One CTA per query row: the row's segment slots each hold at most
+// loose_keep(k) keys, unsorted. They are gathered into shared memory (or, for a
+// row with more candidates than fit, streamed through the thresholded buffer),
+// cut to between k and merge_window(k) keys, sorted, and the first k written
+// out by (value desc, position asc), padded with -1 / 0.
 template <bool kFromLogit>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, int32_t* idx, float* vals) {
   extern __shared__ uint8_t smem_raw[];
@@ -890,6 +941,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
   const int tid = threadIdx.x;
   const int32_t b = blockIdx.x;
   const int32_t* tile_off = reinterpret_cast<const int32_t*>(P.ws);
+  const int keep = loose_keep(P.k), window = merge_window(P.k);
   if (tid == 0) {
     S.sel.n = 0;
     S.sel.tau = 0;
@@ -914,7 +966,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
         const int64_t c = c0 + j;
         if (cta_begin(c, total, P.grid) != cta_begin(c + 1, total, P.grid)) {
           cnt = *reinterpret_cast<const int32_t*>(slot_ptr(j));
-          cnt = cnt < 0 ? 0 : (cnt > P.k ? P.k : cnt);  // a slot never holds more than k keys
+          cnt = cnt < 0 ? 0 : (cnt > keep ? keep : cnt);  // a slot never holds more than loose_keep(k)
         }
       }
       int incl = cnt;
@@ -930,14 +982,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
   }
   __syncthreads();
   const int ntot = S.offs[nslots];
-  int n;
-  if (ntot <= kMergeSort) {
+  if (ntot <= kMergeCap) {
     for (int j = 0; j < nslots; ++j) {
       const int o = S.offs[j], cnt = S.offs[j + 1] - o;
       const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot_ptr(j) + 16);
       for (int i = tid; i < cnt; i += kMergeThreads) S.cand[o + i] = ent[i];
     }
-    n = ntot;
+    if (tid == 0) S.sel.n = static_cast<uint32_t>(ntot);
+    __syncthreads();
   } else {
     for (int j = 0; j < nslots; ++j) {
       const int cnt = S.offs[j + 1] - S.offs[j];
@@ -947,22 +999,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
         const uint64_t tau = S.sel.tau;
         append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
         __syncthreads();
-        shrink_if_above<kMergeThreads>(S.cand, S.scratch, kMergeCap - kMergeThreads, P.k, loose_keep(P.k), &S.sel,
-                                       0, tid);
+        shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, kMergeCap - kMergeThreads, P.k, window, &S.sel, 0,
+                                            tid);
       }
     }
-    shrink_if_above<kMergeThreads>(S.cand, S.scratch, P.k, P.k, P.k, &S.sel, 0, tid);
-    n = static_cast<int>(S.sel.n);
   }
-  int m = 1;
-  while (m < n) m <<= 1;
-  for (int j = n + tid; j < m; j += kMergeThreads) S.cand[j] = 0ull;
-  __syncthreads();
-  if (m > 1) bitonic_sort_desc<kMergeThreads>(S.cand, m, 0, tid);
-  const int kept = n < P.k ? n : P.k;
+  shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, window, P.k, window, &S.sel, 0, tid);
+  const int n = static_cast<int>(S.sel.n);
+  sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
   for (int j = tid; j < P.k; j += kMergeThreads) {
     const int64_t o = static_cast<int64_t>(b) * P.k + j;
-    if (j < kept) {
+    if (j < n) {
       const uint64_t key = S.cand[j];
       const float v = key_value(key);
       idx[o] = key_position(key);
@@ -1044,10 +1091,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_scores_kernel(const Params 
         append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
       }
       __syncthreads();
-      shrink_if_above<kTopkThreads>(S.cand, S.scratch, kCap - kTile, P.k, loose_keep(P.k), &S.sel, 0, tid);
+      shrink_if_above<kTopkThreads, kTopkThreads>(S.cand, S.scratch, kCap - kTile, P.k, loose_keep(P.k), &S.sel, 0,
+                                                  tid);
       const bool seg_end = (i0 + u == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
       if (seg_end) {
-        shrink_if_above<kTopkThreads>(S.cand, S.scratch, P.k, P.k, P.k, &S.sel, 0, tid);
+        shrink_if_above<kTopkThreads, kTopkThreads>(S.cand, S.scratch, loose_keep(P.k), P.k, loose_keep(P.k), &S.sel,
+                                                    0, tid);
         const int n = static_cast<int>(S.sel.n);
         uint8_t* slot = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
         uint64_t* ent = reinterpret_cast<uint64_t*>(slot + 16);
@@ -1081,7 +1130,7 @@ std::mutex g_mu;
 int g_sms[kMaxDevices];
 bool g_ready[kMaxDevices];
 
-size_t slot_bytes_for(int32_t k) { return (16 + 8 * static_cast<size_t>(k) + 15) & ~size_t(15); }
+size_t slot_bytes_for(int32_t k) { return (16 + 8 * static_cast<size_t>(loose_keep(k)) + 15) & ~size_t(15); }
 size_t slots_offset_for(int32_t num_q) { return (4 * (static_cast<size_t>(num_q) + 1) + 255) & ~size_t(255); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

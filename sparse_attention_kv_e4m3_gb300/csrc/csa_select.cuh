@@ -39,12 +39,16 @@ __device__ __forceinline__ int32_t key_position(uint64_t key) {
 __device__ __forceinline__ float key_value(uint64_t key) { return key_float(static_cast<uint32_t>(key >> 32)); }
 
 // Shared scratch of one selecting group.
+constexpr int kCutCandidates = 8;  // thresholds tried per sampled cut
+
 struct SelectShared {
   uint32_t hist[256];
   uint32_t bcast[4];
   uint32_t gather;    // compaction cursor
   uint32_t n;         // live candidates in the buffer
   uint64_t tau;       // admission threshold: a key must exceed it
+  uint64_t cut[kCutCandidates];        // candidate thresholds of a sampled cut, descending
+  uint32_t cut_count[kCutCandidates];  // keys >= each
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -125,24 +129,179 @@ __device__ uint64_t select_kth(const uint64_t* keys, int n, int kk, int max_keep
 
 // Keeps the keys >= T of keys[0, n) (in some order) at the front of `keys`,
 // using `scratch` (room for `cap` keys). Returns their count, at most `cap`
-// (more only if the caller broke the distinct-key precondition).
+// (more only if the caller broke the distinct-key precondition). One shared
+// atomic per warp and round.
 template <int NT>
 __device__ int compact_ge(uint64_t* keys, int n, uint64_t T, uint64_t* scratch, int cap, SelectShared* ss,
                           int bar, int gtid) {
   if (gtid == 0) ss->gather = 0;
   named_bar_sync(bar, NT);
-  for (int i = gtid; i < n; i += NT) {
-    const uint64_t key = keys[i];
-    if (key >= T) {
-      const uint32_t p = atomicAdd(&ss->gather, 1u);
-      if (p < static_cast<uint32_t>(cap)) scratch[p] = key;
-    }
+  for (int base = 0; base < n; base += NT) {
+    const int i = base + gtid;
+    const uint64_t key = i < n ? keys[i] : 0ull;
+    const bool take = i < n && key >= T;
+    const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, take);
+    uint32_t p = 0;
+    if ((gtid & 31) == 0 && ballot) p = atomicAdd(&ss->gather, static_cast<uint32_t>(__popc(ballot)));
+    p = __shfl_sync(0xFFFFFFFFu, p, 0) + __popc(ballot & lanemask_lt());
+    if (take && p < static_cast<uint32_t>(cap)) scratch[p] = key;
   }
   named_bar_sync(bar, NT);
   const int m = min(static_cast<int>(ss->gather), cap);
   for (int i = gtid; i < m; i += NT) keys[i] = scratch[i];
   named_bar_sync(bar, NT);
   return m;
+}
+
+// Sample-guided cut. Tries to find a T with kk <= #(keys[0, n) >= T) <= max_keep
+// and, when it does, moves the keys >= T to the front of `keys` (through
+// `scratch`, room for max(NS / 2, max_keep) keys) and returns T with their count
+// in *kept; otherwise it returns 0 and leaves `keys` alone (the caller falls
+// back to select_kth). The candidate thresholds are value words with a zero
+// position word, T = v << 32, so "key >= T" is "value word >= v" and every test
+// below is a 32-bit compare.
+//
+// NS evenly spaced samples, one per thread of the first NS / 32 warps, are
+// sorted inside each warp (bitonic, by shuffles) and ranked across warps by
+// binary search in the other warps' sorted lists; the sample of rank r has
+// about (r + 1) * n / NS keys at or above it, so the samples whose rank
+// predicts a count between kk and max_keep give kCutCandidates thresholds.
+// One pass counts the keys at or above each; the highest threshold whose count
+// lies in the window wins, and a block-wide scan of each thread's own count
+// places the kept keys without atomics. Keys are nonzero.
+template <int NT, int NS>
+__device__ uint64_t cut_sampled(uint64_t* keys, int n, int kk, int max_keep, uint64_t* scratch, int* kept,
+                                SelectShared* ss, int bar, int gtid) {
+  static_assert(NS % 32 == 0 && NS <= NT && NS <= 256, "one sample per thread of the first NS");
+  constexpr int kC = kCutCandidates, kW = NS / 32;
+  const int lane = gtid & 31, warp = gtid >> 5;
+  uint32_t* sorted = reinterpret_cast<uint32_t*>(scratch);  // kW lists of 32 value words, descending
+  if (gtid < kC) ss->cut_count[gtid] = 0;
+  if (gtid < NS) {
+    uint32_t x = static_cast<uint32_t>(keys[static_cast<int>((static_cast<int64_t>(gtid) * n) / NS)] >> 32);
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int st = size >> 1; st > 0; st >>= 1) {
+        const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, st);
+        const bool keep_max = ((lane & st) == 0) == ((lane & size) == 0);
+        x = keep_max ? max(x, y) : min(x, y);
+      }
+    }
+    sorted[32 * warp + lane] = x;
+  }
+  named_bar_sync(bar, NT);
+  const int lo = max(0, (kk * NS + n - 1) / n - 1);
+  const int hi = max(lo, min(NS - 1, (max_keep * NS) / n - 1));
+  if (gtid < NS) {
+    const uint32_t x = sorted[32 * warp + lane];
+    int r = lane;  // equal words: earlier warps rank above, later ones below
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      if (w == warp) continue;
+      const uint32_t* L = sorted + 32 * w;
+      int a = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) {
+        const uint32_t v = L[a + step - 1];
+        if (w < warp ? v >= x : v > x) a += step;
+      }
+      if (a == 31 && (w < warp ? L[31] >= x : L[31] > x)) a = 32;
+      r += a;
+    }
+#pragma unroll
+    for (int c = 0; c < kC; ++c)
+      if (r == lo + ((hi - lo) * c) / (kC - 1)) ss->cut[c] = static_cast<uint64_t>(x) << 32;
+  }
+  named_bar_sync(bar, NT);
+  uint32_t T[kC], cnt[kC];
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    T[c] = static_cast<uint32_t>(ss->cut[c] >> 32);
+    cnt[c] = 0;
+  }
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(keys) + 1;  // value words, stride 2
+  int i = gtid;
+  for (; i + 3 * NT < n; i += 4 * NT) {
+    uint32_t x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = words[2 * (i + u * NT)];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int c = 0; c < kC; ++c) cnt[c] += x[u] >= T[c] ? 1u : 0u;
+  }
+  for (; i < n; i += NT) {
+    const uint32_t x = words[2 * i];
+#pragma unroll
+    for (int c = 0; c < kC; ++c) cnt[c] += x >= T[c] ? 1u : 0u;
+  }
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, cnt[c]);
+    if (lane == 0 && sum) atomicAdd(&ss->cut_count[c], sum);
+  }
+  named_bar_sync(bar, NT);
+  // thresholds descend with c, so counts ascend: the first count >= kk decides
+  uint32_t best = 0, mine = 0, total = 0;
+  bool found = false;
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    const uint32_t m = ss->cut_count[c];
+    if (!found && m >= static_cast<uint32_t>(kk)) {
+      found = true;
+      if (m <= static_cast<uint32_t>(max_keep)) {
+        best = T[c];
+        mine = cnt[c];
+        total = m;
+      }
+    }
+  }
+  if (best == 0) return 0ull;  // uniform
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) ss->hist[warp] = incl;
+  named_bar_sync(bar, NT);
+  uint32_t p = incl - mine;
+  for (int w = 0; w < warp; ++w) p += ss->hist[w];
+  i = gtid;
+  for (; i + 3 * NT < n; i += 4 * NT) {
+    uint64_t x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = keys[i + u * NT];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (static_cast<uint32_t>(x[u] >> 32) >= best) scratch[p++] = x[u];
+  }
+  for (; i < n; i += NT) {
+    const uint64_t x = keys[i];
+    if (static_cast<uint32_t>(x >> 32) >= best) scratch[p++] = x;
+  }
+  named_bar_sync(bar, NT);
+  for (int j = gtid; j < static_cast<int>(total); j += NT) keys[j] = scratch[j];
+  named_bar_sync(bar, NT);
+  *kept = static_cast<int>(total);
+  return static_cast<uint64_t>(best) << 32;
+}
+
+// Every thread offers two keys (`take_a`, `take_b`); accepted keys are appended
+// to buf at ss->n with one shared atomic per warp. The caller's group barrier
+// makes ss->n current.
+__device__ __forceinline__ void append_keys2(uint64_t* buf, uint64_t a, bool take_a, uint64_t b, bool take_b,
+                                             SelectShared* ss) {
+  const uint32_t ba = __ballot_sync(0xFFFFFFFFu, take_a);
+  const uint32_t bb = __ballot_sync(0xFFFFFFFFu, take_b);
+  const uint32_t na = __popc(ba);
+  uint32_t base = 0;
+  if ((threadIdx.x & 31) == 0 && (ba | bb)) base = atomicAdd(&ss->n, na + static_cast<uint32_t>(__popc(bb)));
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  const uint32_t lt = lanemask_lt();
+  if (take_a) buf[base + __popc(ba & lt)] = a;
+  if (take_b) buf[base + na + __popc(bb & lt)] = b;
 }
 
 // Every thread offers at most one key (`take`); accepted keys are appended to
@@ -159,14 +318,22 @@ __device__ __forceinline__ void append_key(uint64_t* buf, uint64_t key, bool tak
 // for a T that keeps between kk and max_keep of them (exactly the kk best when
 // max_keep == kk), and raises the admission threshold to T. Any such T is a
 // valid threshold: at least kk keys seen so far are >= T, so no key below T can
-// be among the kk best. Group-uniform.
-template <int NT>
-__device__ void shrink_if_above(uint64_t* buf, uint64_t* scratch, int limit, int kk, int max_keep, SelectShared* ss,
+// be among the kk best. The sampled cut is tried first when the window is
+// open; `scratch` holds max(NS, max_keep) keys. Group-uniform. Kept out of
+// line: cuts are rare, and one copy of their code leaves more of the
+// instruction cache to the loops that run every tile.
+template <int NT, int NS>
+__device__ __noinline__ void shrink_if_above(uint64_t* buf, uint64_t* scratch, int limit, int kk, int max_keep, SelectShared* ss,
                                 int bar, int gtid) {
   const int n = static_cast<int>(ss->n);
   if (n <= limit || n <= kk) return;
-  const uint64_t T = select_kth<NT>(buf, n, kk, max_keep, ss, bar, gtid);
-  const int m = compact_ge<NT>(buf, n, T, scratch, max_keep, ss, bar, gtid);
+  uint64_t T = 0;
+  int m = 0;
+  if (max_keep > kk) T = cut_sampled<NT, NS>(buf, n, kk, max_keep, scratch, &m, ss, bar, gtid);
+  if (T == 0) {
+    T = select_kth<NT>(buf, n, kk, max_keep, ss, bar, gtid);
+    m = compact_ge<NT>(buf, n, T, scratch, max_keep, ss, bar, gtid);
+  }
   if (gtid == 0) {
     ss->n = static_cast<uint32_t>(m);
     ss->tau = T ? T - 1 : 0;  // admit keys > T - 1, i.e. >= T; later keys are new (distinct)
@@ -192,6 +359,85 @@ __device__ void bitonic_sort_desc(uint64_t* keys, int m, int bar, int gtid) {
       named_bar_sync(bar, NT);
     }
   }
+}
+
+// One compare-exchange stage over register pairs: thread t holds positions
+// 2t and 2t + 1 in (a, b); stride st >= 2 pairs them with thread t ^ (st / 2)
+// of the same warp, stride 1 with each other. Blocks of `size` positions are
+// ordered descending or ascending alternately, as the bitonic network wants.
+__device__ __forceinline__ void pair_stage(uint64_t& a, uint64_t& b, int t, int size, int st) {
+  const bool desc = ((2 * t) & size) == 0;
+  if (st == 1) {
+    if (desc ? (a < b) : (a > b)) {
+      const uint64_t x = a;
+      a = b;
+      b = x;
+    }
+    return;
+  }
+  const int ts = st >> 1;
+  const uint64_t pa = __shfl_xor_sync(0xFFFFFFFFu, a, ts);
+  const uint64_t pb = __shfl_xor_sync(0xFFFFFFFFu, b, ts);
+  const bool keep_max = ((t & ts) == 0) == desc;
+  a = keep_max ? (a > pa ? a : pa) : (a < pa ? a : pa);
+  b = keep_max ? (b > pb ? b : pb) : (b < pb ? b : pb);
+}
+
+// Sorts keys[0, n) in descending order in place; keys[n, m) are overwritten with
+// zero padding, where m is the power of two >= max(n, 64) (the buffer must hold
+// m keys). When m <= 2 * NT each thread keeps two keys in registers: every
+// stage with stride below 64 runs on shuffles, and only the longer strides go
+// through shared memory with a barrier each.
+template <int NT>
+__device__ void sort_prefix_desc(uint64_t* keys, int n, int bar, int gtid) {
+  int m = 64;
+  while (m < n) m <<= 1;
+  for (int j = n + gtid; j < m; j += NT) keys[j] = 0ull;
+  named_bar_sync(bar, NT);
+  if (m > 2 * NT) {
+    bitonic_sort_desc<NT>(keys, m, bar, gtid);
+    return;
+  }
+  const int t = gtid;
+  const bool act = t < (m >> 1);  // whole warps: m / 2 >= 32
+  uint64_t a = 0, b = 0;
+  if (act) {
+    a = keys[2 * t];
+    b = keys[2 * t + 1];
+  }
+  for (int size = 2; size <= m; size <<= 1) {
+    int st = size >> 1;
+    if (st >= 64) {
+      if (act) {
+        keys[2 * t] = a;
+        keys[2 * t + 1] = b;
+      }
+      named_bar_sync(bar, NT);
+      for (; st >= 64; st >>= 1) {
+        if (act) {
+          const int lo = 2 * t - (t & (st - 1));
+          const int hi = lo + st;
+          const uint64_t x = keys[lo], y = keys[hi];
+          const bool desc = (lo & size) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            keys[lo] = y;
+            keys[hi] = x;
+          }
+        }
+        named_bar_sync(bar, NT);
+      }
+      if (act) {
+        a = keys[2 * t];
+        b = keys[2 * t + 1];
+      }
+    }
+    for (; st > 0; st >>= 1) pair_stage(a, b, t, size, st);
+  }
+  if (act) {
+    keys[2 * t] = a;
+    keys[2 * t + 1] = b;
+  }
+  named_bar_sync(bar, NT);
 }
 
 }  // namespace csa

@@ -63,7 +63,9 @@ def test_workspace_bytes_is_host_arithmetic(lib):
     a = native.Args()
     a.num_q = 64
     slots = 64 + native.MAX_CTAS
-    assert native.workspace_bytes(a, 512) == 512 + slots * (16 + 8 * 512)
+    # a slot holds up to min(1024, k + k/2) keys of 8 bytes after a 16-byte header
+    assert native.workspace_bytes(a, 512) == 512 + slots * (16 + 8 * 768)
+    assert native.workspace_bytes(a, 1000) == 512 + slots * (16 + 8 * 1024)
     assert native.workspace_bytes(a, 0) == 0
     assert native.workspace_bytes(a, native.MAX_K + 1) == 0
     a.num_q = -1
