@@ -918,9 +918,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
 
 // ------------------------------------------------------------------ merge
 
-constexpr int kMergeThreads = 512;
-constexpr int kMergeCap = 8192;   // candidate buffer of the general path
+// A merge CTA is small so that several rows run on each SM: the merge is
+// latency-bound (a few dependent global reads, then shared-memory passes).
+constexpr int kMergeThreads = 256;
+constexpr int kMergeCap = 4096;   // candidate buffer; a row with more is cut back between chunks of slots
 constexpr int kMergeSlots = CSA_MAX_CTAS + 1;
+static_assert(2 * CSA_MAX_K <= kMergeCap, "after a cut to merge_window(k), any slot must fit");
 
 struct MergeSmem {
   uint64_t cand[kMergeCap];
@@ -930,10 +933,10 @@ struct MergeSmem {
 };
 
 // One CTA per query row: the row's segment slots each hold at most
-// loose_keep(k) keys, unsorted. They are gathered into shared memory (or, for a
-// row with more candidates than fit, streamed through the thresholded buffer),
-// cut to between k and merge_window(k) keys, sorted, and the first k written
-// out by (value desc, position asc), padded with -1 / 0.
+// loose_keep(k) keys, unsorted. They are gathered into shared memory (a row
+// with more candidates than fit is cut back between chunks of slots), cut to
+// between k and merge_window(k) keys, sorted, and the first k written out by
+// (value desc, position asc), padded with -1 / 0.
 template <bool kFromLogit>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, int32_t* idx, float* vals) {
   extern __shared__ uint8_t smem_raw[];
@@ -981,31 +984,40 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
     if (tid == 0) S.offs[nslots] = run;
   }
   __syncthreads();
-  const int ntot = S.offs[nslots];
-  if (ntot <= kMergeCap) {
-    for (int j = 0; j < nslots; ++j) {
+  // Gather whole slots while they fit, one warp per slot with four loads in
+  // flight per lane; when the next slot would not fit, cut the buffer to at
+  // most `window` keys (never below k) and go on. After a cut any slot fits:
+  // window + loose_keep(k) <= 2 * CSA_MAX_K <= kMergeCap.
+  const int warp = tid >> 5, lane = tid & 31;
+  int n = 0;
+  for (int j0 = 0; j0 < nslots;) {
+    int j1 = j0;
+    while (j1 < nslots && n + (S.offs[j1 + 1] - S.offs[j0]) <= kMergeCap) ++j1;
+    const int base = n - S.offs[j0];
+    for (int j = j0 + warp; j < j1; j += kMergeThreads / 32) {
       const int o = S.offs[j], cnt = S.offs[j + 1] - o;
       const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot_ptr(j) + 16);
-      for (int i = tid; i < cnt; i += kMergeThreads) S.cand[o + i] = ent[i];
-    }
-    if (tid == 0) S.sel.n = static_cast<uint32_t>(ntot);
-    __syncthreads();
-  } else {
-    for (int j = 0; j < nslots; ++j) {
-      const int cnt = S.offs[j + 1] - S.offs[j];
-      const uint64_t* ent = reinterpret_cast<const uint64_t*>(slot_ptr(j) + 16);
-      for (int base = 0; base < cnt; base += kMergeThreads) {
-        const uint64_t key = (base + tid < cnt) ? ent[base + tid] : 0ull;
-        const uint64_t tau = S.sel.tau;
-        append_key(S.cand, key, key != 0ull && key > tau, &S.sel);
-        __syncthreads();
-        shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, kMergeCap - kMergeThreads, P.k, window, &S.sel, 0,
-                                            tid);
+      uint64_t* dst = S.cand + base + o;
+      for (int i = lane; i < cnt; i += 128) {
+        uint64_t v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = (i + 32 * u < cnt) ? ent[i + 32 * u] : 0ull;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i + 32 * u < cnt) dst[i + 32 * u] = v[u];
       }
+    }
+    n += S.offs[j1] - S.offs[j0];
+    j0 = j1;
+    if (tid == 0) S.sel.n = static_cast<uint32_t>(n);
+    __syncthreads();
+    if (j0 < nslots) {
+      shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, window, P.k, window, &S.sel, 0, tid);
+      n = static_cast<int>(S.sel.n);
     }
   }
   shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, window, P.k, window, &S.sel, 0, tid);
-  const int n = static_cast<int>(S.sel.n);
+  n = static_cast<int>(S.sel.n);
   sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
   for (int j = tid; j < P.k; j += kMergeThreads) {
     const int64_t o = static_cast<int64_t>(b) * P.k + j;

@@ -361,83 +361,92 @@ __device__ void bitonic_sort_desc(uint64_t* keys, int m, int bar, int gtid) {
   }
 }
 
-// One compare-exchange stage over register pairs: thread t holds positions
-// 2t and 2t + 1 in (a, b); stride st >= 2 pairs them with thread t ^ (st / 2)
-// of the same warp, stride 1 with each other. Blocks of `size` positions are
-// ordered descending or ascending alternately, as the bitonic network wants.
-__device__ __forceinline__ void pair_stage(uint64_t& a, uint64_t& b, int t, int size, int st) {
-  const bool desc = ((2 * t) & size) == 0;
-  if (st == 1) {
-    if (desc ? (a < b) : (a > b)) {
-      const uint64_t x = a;
-      a = b;
-      b = x;
-    }
-    return;
+// Orders (a, b) descending when desc, ascending otherwise.
+__device__ __forceinline__ void cex(uint64_t& a, uint64_t& b, bool desc) {
+  if (desc ? (a < b) : (a > b)) {
+    const uint64_t x = a;
+    a = b;
+    b = x;
   }
-  const int ts = st >> 1;
-  const uint64_t pa = __shfl_xor_sync(0xFFFFFFFFu, a, ts);
-  const uint64_t pb = __shfl_xor_sync(0xFFFFFFFFu, b, ts);
-  const bool keep_max = ((t & ts) == 0) == desc;
-  a = keep_max ? (a > pa ? a : pa) : (a < pa ? a : pa);
-  b = keep_max ? (b > pb ? b : pb) : (b < pb ? b : pb);
+}
+
+// Bitonic sort of keys[0, m) into descending order, E consecutive keys per
+// thread in registers (the first m / E threads, whole warps): strides below E
+// inside a thread, strides from E to 16E by shuffles within the warp, longer
+// strides through shared memory with one barrier each. m is a power of two,
+// 32E <= m <= E * NT.
+template <int NT, int E>
+__device__ void sort_regs_desc(uint64_t* keys, int m, int bar, int gtid) {
+  const int t = gtid;
+  const bool act = t < m / E;
+  uint64_t v[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) v[i] = act ? keys[E * t + i] : 0ull;
+  for (int size = 2; size <= m; size <<= 1) {
+    int st = size >> 1;
+    if (st >= 32 * E) {
+      if (act) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) keys[E * t + i] = v[i];
+      }
+      named_bar_sync(bar, NT);
+      for (; st >= 32 * E; st >>= 1) {
+        for (int u = t; u < (m >> 1); u += NT) {
+          const int lo = 2 * u - (u & (st - 1));
+          uint64_t x = keys[lo], y = keys[lo + st];
+          cex(x, y, (lo & size) == 0);
+          keys[lo] = x;
+          keys[lo + st] = y;
+        }
+        named_bar_sync(bar, NT);
+      }
+      if (act) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) v[i] = keys[E * t + i];
+      }
+    }
+    for (; st >= E; st >>= 1) {  // partner thread t ^ (st / E), same warp
+      const int ts = st / E;
+      const bool keep_max = ((t & ts) == 0) == (((E * t) & size) == 0);
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const uint64_t pv = __shfl_xor_sync(0xFFFFFFFFu, v[i], ts);
+        v[i] = keep_max ? (v[i] > pv ? v[i] : pv) : (v[i] < pv ? v[i] : pv);
+      }
+    }
+#pragma unroll
+    for (int sc = E / 2; sc > 0; sc >>= 1) {  // inside the thread
+      if (sc <= st) {
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+          if ((i & sc) == 0) cex(v[i], v[i + sc], (((E * t + i) & size) == 0));
+      }
+    }
+  }
+  if (act) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) keys[E * t + i] = v[i];
+  }
+  named_bar_sync(bar, NT);
 }
 
 // Sorts keys[0, n) in descending order in place; keys[n, m) are overwritten with
 // zero padding, where m is the power of two >= max(n, 64) (the buffer must hold
-// m keys). When m <= 2 * NT each thread keeps two keys in registers: every
-// stage with stride below 64 runs on shuffles, and only the longer strides go
-// through shared memory with a barrier each.
+// m keys). Up to 8 * NT keys are sorted in registers (sort_regs_desc).
 template <int NT>
 __device__ void sort_prefix_desc(uint64_t* keys, int n, int bar, int gtid) {
   int m = 64;
   while (m < n) m <<= 1;
   for (int j = n + gtid; j < m; j += NT) keys[j] = 0ull;
   named_bar_sync(bar, NT);
-  if (m > 2 * NT) {
+  if (m <= 2 * NT)
+    sort_regs_desc<NT, 2>(keys, m, bar, gtid);
+  else if (m <= 4 * NT)
+    sort_regs_desc<NT, 4>(keys, m, bar, gtid);
+  else if (m <= 8 * NT)
+    sort_regs_desc<NT, 8>(keys, m, bar, gtid);
+  else
     bitonic_sort_desc<NT>(keys, m, bar, gtid);
-    return;
-  }
-  const int t = gtid;
-  const bool act = t < (m >> 1);  // whole warps: m / 2 >= 32
-  uint64_t a = 0, b = 0;
-  if (act) {
-    a = keys[2 * t];
-    b = keys[2 * t + 1];
-  }
-  for (int size = 2; size <= m; size <<= 1) {
-    int st = size >> 1;
-    if (st >= 64) {
-      if (act) {
-        keys[2 * t] = a;
-        keys[2 * t + 1] = b;
-      }
-      named_bar_sync(bar, NT);
-      for (; st >= 64; st >>= 1) {
-        if (act) {
-          const int lo = 2 * t - (t & (st - 1));
-          const int hi = lo + st;
-          const uint64_t x = keys[lo], y = keys[hi];
-          const bool desc = (lo & size) == 0;
-          if (desc ? (x < y) : (x > y)) {
-            keys[lo] = y;
-            keys[hi] = x;
-          }
-        }
-        named_bar_sync(bar, NT);
-      }
-      if (act) {
-        a = keys[2 * t];
-        b = keys[2 * t + 1];
-      }
-    }
-    for (; st > 0; st >>= 1) pair_stage(a, b, t, size, st);
-  }
-  if (act) {
-    keys[2 * t] = a;
-    keys[2 * t + 1] = b;
-  }
-  named_bar_sync(bar, NT);
 }
 
 }  // namespace csa
