@@ -618,22 +618,19 @@ __device__ void role_worker(const Params& P, Smem& S) {
   // when the record is not visible) and the record's logical position.
   auto load = [&](int64_t i, uint32_t (&sc)[kSub], uint32_t (&pos)[kSub]) -> bool {
     const int ta = static_cast<int>(i % kAStages);
-    bool ok = true;
-    if (lane == 0) {
-      ok = mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag);
+    // every lane waits, and so acquires the pages itself: no divergent branch, no broadcast
+    bool ok = mbar_wait(smem_u32(&S.aempty[ta]), static_cast<uint32_t>(((i / kAStages) & 1) ^ 1), &S.abort_flag);
 #pragma unroll
-      for (int sub = 0; sub < kSub; ++sub) {
-        const int64_t pg = kTilePages * i + 2 * sub + half;
-        ok = ok && mbar_wait(smem_u32(&S.full[pg % kStages]), static_cast<uint32_t>((pg / kStages) & 1),
-                             &S.abort_flag);
-      }
+    for (int sub = 0; sub < kSub; ++sub) {
+      const int64_t pg = kTilePages * i + 2 * sub + half;
+      ok = ok && mbar_wait(smem_u32(&S.full[pg % kStages]), static_cast<uint32_t>((pg / kStages) & 1),
+                           &S.abort_flag);
     }
-    if (!warp_ok(ok)) return false;
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
 #pragma unroll
     for (int sub = 0; sub < kSub; ++sub) {
       const int64_t pg = kTilePages * i + 2 * sub + half;
       const int s = static_cast<int>(pg % kStages);
-      mbar_wait_drain(smem_u32(&S.full[s]), static_cast<uint32_t>((pg / kStages) & 1));  // acquire
       const PageInfo e = S.info[s];
       const uint8_t* src = S.pages[s] + r * kRec;
       uint32_t v[32];
@@ -708,11 +705,9 @@ __device__ void role_worker(const Params& P, Smem& S) {
         if (!isnan(__uint_as_float(sc[sub]))) out[kMmaRows * sub] = __frcp_rn(1.0f + __expf(-logit[sub]));
     } else {
       const int slot = static_cast<int>(i % kKeyRing);
-      bool ok2 = true;
-      if (lane == 0)
-        ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
-                        &S.abort_flag);
-      if (!warp_ok(ok2)) return false;
+      const bool ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
+                                 &S.abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, ok2)) return false;
       // keys that can still make the segment's best k, packed into this warp's region
       const uint32_t thr = filter_word(S, seg);
       const uint32_t lt = lanemask_lt();
@@ -750,19 +745,14 @@ __device__ void role_worker(const Params& P, Smem& S) {
     const bool seg_end = (t == nt - 1) || (cur.lt == cur.tiles - 1);
     if (t % kWorkerGroups == group) {
       if (seg != wseg) {  // first own tile of this segment: its head weights must be ready
-        bool okq = true;
-        if (lane == 0)
-          okq = mbar_wait(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag);
-        if (!warp_ok(okq)) break;
-        mbar_wait_drain(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1));
+        const bool okq = mbar_wait(smem_u32(&S.qfull[seg & 1]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, okq)) break;
         wseg = seg;
       }
       // MMA of tile t done: its accumulator is ready and the group's key stage is free
-      bool okd = true;
-      if (lane == 0)
-        okd = mbar_wait(smem_u32(&S.dfull[t % kDStages]), static_cast<uint32_t>((t / kDStages) & 1),
-                        &S.abort_flag);
-      if (!warp_ok(okd)) break;
+      const bool okd = mbar_wait(smem_u32(&S.dfull[t % kDStages]), static_cast<uint32_t>((t / kDStages) & 1),
+                                 &S.abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, okd)) break;
       if (t + kWorkerGroups < nt) {
         ok = load(t + kWorkerGroups, nxt_sc, nxt_pos);
         if (!ok) break;
