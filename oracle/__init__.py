@@ -9,7 +9,9 @@ What it computes (FlashMemory-DeepSeek-V4, "Retriever architecture" and
     k      = e4m3(record[:128]) * fp32(record[128:132])
     logit  = sum_h relu(k . q_h) * fused_w_h
     score  = sigmoid(logit)
-and the top-k records of each query by (logit desc, position asc).
+and the top-k records of each query by (logit desc, position asc); and the
+compressed-K writer that produces such records from key rows (scale = amax/448,
+codes = nearest e4m3 of x / scale in binary32).
 """
 from __future__ import annotations
 
@@ -28,6 +30,7 @@ _lib = None
 
 PAGE_OOB = 1
 RESIDENT_OOB = 2
+RANGE = 4
 BAD_REQUEST = 16
 LEN_OOB = 32
 
@@ -91,6 +94,16 @@ def _bind(path: str):
     lib.oracle_topk_sample.restype = ctypes.c_int64
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int32
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode_many.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    lib.oracle_e4m3_encode_many.restype = None
+    lib.oracle_quantise_row.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_quantise_row.restype = ctypes.c_int32
+    lib.oracle_write_keys.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_int32, ctypes.c_int32]
+    lib.oracle_write_keys.restype = ctypes.c_int32
     return lib
 
 
@@ -180,6 +193,15 @@ class Oracle:
 
     def topk(self, problem: Problem, k: int):
         return _topk(self.lib, problem, k)
+
+    def e4m3_encode(self, values) -> np.ndarray:
+        return _e4m3_encode(self.lib, values)
+
+    def quantise_row(self, x):
+        return _quantise_row(self.lib, x)
+
+    def write_keys(self, keys, req, pos, kv, page_table) -> int:
+        return _write_keys(self.lib, keys, req, pos, kv, page_table)
 
 
 def load_build(path: str) -> Oracle:
@@ -275,3 +297,46 @@ def topk_sample(problem: Problem, b0: int, b1: int, max_records: int, k: int):
 
 def threads() -> int:
     return int(_load().oracle_threads())
+
+
+def _e4m3_encode(lib, values) -> np.ndarray:
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib.oracle_e4m3_encode_many(v.ctypes.data, int(v.size), out.ctypes.data)
+    return out
+
+
+def _quantise_row(lib, x):
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    assert v.shape == (128,)
+    rec = np.zeros(132, dtype=np.uint8)
+    flags = lib.oracle_quantise_row(v.ctypes.data, rec.ctypes.data)
+    return rec, int(flags)
+
+
+def _write_keys(lib, keys, req, pos, kv, page_table) -> int:
+    """Writes key rows into `kv` ([num_pages, page_stride] uint8, C-contiguous) in
+    place; returns the OR of the flag bits."""
+    k = np.ascontiguousarray(keys, dtype=np.float32)
+    assert k.ndim == 2 and k.shape[1] == 128
+    assert kv.dtype == np.uint8 and kv.flags["C_CONTIGUOUS"]
+    p = np.ascontiguousarray(pos, dtype=np.int32)
+    r = None if req is None else np.ascontiguousarray(req, dtype=np.int32)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    return int(lib.oracle_write_keys(k.ctypes.data, int(k.shape[0]), _ptr(r), p.ctypes.data, kv.ctypes.data,
+                                     int(kv.shape[0]), int(kv.shape[1]), pt.ctypes.data, int(pt.shape[0]),
+                                     int(pt.shape[1])))
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """binary32 values -> e4m3 codes (nearest, ties to even, saturating at 448)."""
+    return _e4m3_encode(_load(), values)
+
+
+def quantise_row(x):
+    """One key row of 128 binary32 values -> (132-byte record, flags)."""
+    return _quantise_row(_load(), x)
+
+
+def write_keys(keys, req, pos, kv, page_table) -> int:
+    return _write_keys(_load(), keys, req, pos, kv, page_table)

@@ -43,6 +43,7 @@
 /* Flag bits reported by the oracle (the oracle's own numbering). */
 #define OR_FLAG_PAGE_OOB 1
 #define OR_FLAG_RESIDENT_OOB 2
+#define OR_FLAG_RANGE 4
 #define OR_FLAG_BAD_REQUEST 16
 #define OR_FLAG_LEN_OOB 32
 
@@ -351,4 +352,109 @@ int32_t oracle_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/* ------------------------------------------------------------------ writer
+ *
+ * The compressed-K writer, the step before the path: it quantises new key rows
+ * into the record format and stores them in the paged cache.
+ * FlashMemory-DeepSeek-V4, "compressed_k format" fixes the record (HEAD_DIM e4m3
+ * bytes, then the fp32 scale; k = e4m3 * scale); the BatchGen #153 commit log
+ * names a store kernel that writes the indexer pool in that [128B fp8 | 4B fp32
+ * scale] layout. The scale and the rounding are the plainest reading of that
+ * format and of the workloads' "fp32 scale = amax/448" (448 = largest e4m3):
+ *   amax  = max_d |x_d|                      (exact)
+ *   scale = amax / 448                       (binary32 division, nearest even)
+ *   c_d   = e4m3(x_d / scale)                (x_d / scale in binary32, then the
+ *                                            nearest e4m3 value, ties to the even
+ *                                            mantissa; magnitudes past 448 saturate)
+ *   a row with amax == 0 is stored as zero codes and scale 0.
+ * The code is decided in binary32, the precision of the pages' torch cast.
+ */
+
+/* binary32 -> OCP E4M3 "fn" byte: the nearest of the 127 non-negative finite
+ * e4m3 values (searched one by one), ties to the even mantissa, with the sign of
+ * the input. Values beyond 448 get 448 (the largest value is the nearest). NaN
+ * gives the NaN code 0x7F. */
+uint8_t oracle_e4m3_encode(float v) {
+  if (isnan(v)) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs((double)v);
+  int best = 0;
+  double best_d = a;  /* distance to code 0 (value 0) */
+  for (int c = 1; c < 127; ++c) {
+    const double d = fabs(a - oracle_e4m3((uint8_t)c));
+    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+void oracle_e4m3_encode_many(const float* v, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+/* One record from one row of OR_D binary32 values; returns OR_FLAG_RANGE (and
+ * writes nothing) if a value is not finite. */
+int32_t oracle_quantise_row(const float* x, uint8_t* rec) {
+  float amax = 0.0f;
+  for (int d = 0; d < OR_D; ++d) {
+    if (!isfinite(x[d])) return OR_FLAG_RANGE;
+    const float a = fabsf(x[d]);
+    if (a > amax) amax = a;
+  }
+  const float scale = amax / 448.0f;
+  for (int d = 0; d < OR_D; ++d) {
+    if (amax == 0.0f) {
+      rec[d] = 0;
+    } else {
+      const float y = x[d] / scale;
+      rec[d] = oracle_e4m3_encode(y);
+    }
+  }
+  uint32_t bits;
+  memcpy(&bits, &scale, 4);
+  for (int j = 0; j < 4; ++j) rec[OR_D + j] = (uint8_t)(bits >> (8 * j));  /* little-endian */
+  return 0;
+}
+
+/*
+ * Writes n rows into the cache in place. keys [n, OR_D] binary32 (bf16 rows are
+ * widened exactly by the caller); row i goes to request req[i] (req NULL: request
+ * i) at logical position pos[i]: physical page page_table[req][pos / 64], record
+ * pos % 64. A row with a request outside [0, num_req), a position outside
+ * [0, 64 * pt_stride), a physical page outside [0, num_pages) or a non-finite
+ * value is skipped and flagged. Returns the OR of the flags.
+ */
+int32_t oracle_write_keys(const float* keys, int64_t n, const int32_t* req, const int32_t* pos, uint8_t* kv,
+                          int64_t num_pages, int64_t page_stride, const int32_t* page_table, int32_t num_req,
+                          int32_t pt_stride) {
+  int32_t flags = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t r = req ? req[i] : i;
+    if (r < 0 || r >= num_req) {
+      flags |= OR_FLAG_BAD_REQUEST;
+      continue;
+    }
+    const int64_t p = pos[i];
+    if (p < 0 || p >= (int64_t)OR_PAGE * pt_stride) {
+      flags |= OR_FLAG_LEN_OOB;
+      continue;
+    }
+    const int64_t phys = page_table[r * pt_stride + p / OR_PAGE];
+    if (phys < 0 || phys >= num_pages) {
+      flags |= OR_FLAG_PAGE_OOB;
+      continue;
+    }
+    uint8_t rec[OR_REC_BYTES];
+    const int32_t f = oracle_quantise_row(keys + i * OR_D, rec);
+    if (f) {
+      flags |= f;
+      continue;
+    }
+    memcpy(kv + phys * page_stride + (p % OR_PAGE) * OR_REC_BYTES, rec, OR_REC_BYTES);
+  }
+  return flags;
 }

@@ -370,4 +370,116 @@ def pin_invalid_geometry(o: O.Oracle):
     assert fr & O.RESIDENT_OOB and len(posr) == min(64, 300 - 64 * int(r.resident[0, 0]))
 
 
+# ---------------------------------------------------------------- compressed-K writer
+#
+# The writer quantises key rows into records (scale = amax/448 in binary32, codes
+# = nearest e4m3 of x / scale, ties to even). Its pins tie it to torch's e4m3 cast,
+# to the workload generator's own records, to closed forms and to the geometry.
+
+def _torch_decode(codes) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float32).numpy()
+
+
+def _torch_encode(v) -> np.ndarray:
+    t = torch.as_tensor(np.ascontiguousarray(v, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def pin_writer_encode_round_trip(o: O.Oracle):
+    """Every finite e4m3 value encodes back to its own byte (signed zero too)."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    got = o.e4m3_encode(_torch_decode(codes))
+    assert np.array_equal(got, codes), codes[got != codes]
+
+
+def pin_writer_encode_vs_torch(o: O.Oracle):
+    """Nearest with ties to even, as torch's cast: at every midpoint between
+    neighbouring values, one binary32 step to either side of it, and on random
+    values from the subnormal range to 448."""
+    vals = np.sort(_torch_decode(np.arange(0, 127, dtype=np.uint8)))
+    mid = ((vals[:-1].astype(np.float64) + vals[1:]) / 2).astype(np.float32)
+    probes = np.concatenate([mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(1e9))])
+    rng = np.random.default_rng(11)
+    rnd = (2.0 ** rng.uniform(-12, np.log2(448.0), 20000)).astype(np.float32)
+    probes = np.concatenate([probes, rnd, vals])
+    probes = np.concatenate([probes, -probes])
+    assert np.array_equal(o.e4m3_encode(probes), _torch_encode(probes))
+
+
+def pin_writer_matches_generator(o: O.Oracle):
+    """The workload generator quantises its keys with numpy and torch; quantising
+    the same drawn rows with the oracle gives the same 132-byte records."""
+    w = synth.make_workload("wgen", num_q=1, history=[2 * PAGE], shuffle=False, seed=5, threads=1)
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(5, spawn_key=(1, 0))))
+    x = g.standard_normal((2, PAGE, D), dtype=np.float32)
+    for p in range(2):
+        for r in range(PAGE):
+            rec, flags = o.quantise_row(x[p, r])
+            assert flags == 0
+            assert np.array_equal(rec, w.kv[p, r * REC:(r + 1) * REC]), (p, r)
+
+
+def pin_writer_closed_forms(o: O.Oracle):
+    # zero row: zero codes and zero scale
+    rec, _ = o.quantise_row(np.zeros(D, np.float32))
+    assert not rec.any()
+    # a row on the e4m3 grid whose largest magnitude is 448: scale 1, exact codes
+    codes = np.random.default_rng(3).integers(0, 126, D).astype(np.uint8)
+    codes[7] = 0x7E
+    codes[::3] |= 0x80
+    x = _torch_decode(codes)
+    rec, _ = o.quantise_row(x)
+    assert struct.unpack("<f", rec[D:].tobytes())[0] == 1.0 and np.array_equal(rec[:D], codes)
+    # scaling by a power of two keeps the codes and scales the scale
+    for e in (-20, -3, 5, 30):
+        rec2, _ = o.quantise_row((x * np.float32(2.0 ** e)).astype(np.float32))
+        assert np.array_equal(rec2[:D], codes)
+        assert struct.unpack("<f", rec2[D:].tobytes())[0] == 2.0 ** e
+    # a single nonzero value v: code +-448 and scale |v| / 448 in binary32
+    for v in (3.0, -0.015625, 1234.5):
+        row = np.zeros(D, np.float32)
+        row[17] = v
+        rec, _ = o.quantise_row(row)
+        assert rec[17] == (0xFE if v < 0 else 0x7E) and not np.delete(rec[:D], 17).any()
+        assert struct.unpack("<f", rec[D:].tobytes())[0] == np.float32(abs(v)) / np.float32(448.0)
+
+
+def pin_writer_error_bound(o: O.Oracle):
+    """decode(code) * scale is within half a code step of x / scale, times scale."""
+    x = np.random.default_rng(8).standard_normal((40, D)).astype(np.float32) * np.float32(7.0)
+    for row in x:
+        rec, _ = o.quantise_row(row)
+        s = struct.unpack("<f", rec[D:].tobytes())[0]
+        y = row.astype(np.float64) / s
+        back = _torch_decode(rec[:D]).astype(np.float64)
+        step = np.where(np.abs(y) >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 1e-30))) - 3), 2.0 ** -9)
+        assert np.all(np.abs(back - y) <= step / 2 * (1 + 1e-6))
+
+
+def pin_writer_geometry(o: O.Oracle):
+    """Rows land at page_table[req][pos // 64], record pos % 64; nothing else is
+    touched; invalid rows are skipped and flagged."""
+    kv = np.full((4, PAGE * REC + 16), 0xA5, dtype=np.uint8)
+    pt = np.array([[2, 0], [3, 1]], dtype=np.int32)
+    rows = np.random.default_rng(4).standard_normal((6, D)).astype(np.float32)
+    rows[5, 3] = np.nan
+    req = np.array([0, 1, 7, 0, 1, 1], dtype=np.int32)
+    pos = np.array([70, 5, 0, 128, 64, 9], dtype=np.int32)
+    flags = o.write_keys(rows, req, pos, kv, pt)
+    assert flags == O.BAD_REQUEST | O.LEN_OOB | O.RANGE, flags
+    want = np.full_like(kv, 0xA5)
+    for i, (page, r) in ((0, (0, 6)), (1, (3, 5)), (4, (1, 0))):
+        want[page, r * REC:(r + 1) * REC] = o.quantise_row(rows[i])[0]
+    assert np.array_equal(kv, want)
+    # identity request map; a page id out of range
+    kv2 = np.full_like(kv, 0xA5)
+    pt2 = np.array([[1], [9]], dtype=np.int32)
+    flags = o.write_keys(rows[:2], None, np.array([3, 2], np.int32), kv2, pt2)
+    assert flags == O.PAGE_OOB
+    want = np.full_like(kv, 0xA5)
+    want[1, 3 * REC:4 * REC] = o.quantise_row(rows[0])[0]
+    assert np.array_equal(kv2, want)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

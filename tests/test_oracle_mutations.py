@@ -36,6 +36,19 @@ MUTATIONS = [
      "if (score) score[o] = 0.5;\n        if (logit) logit[o] = -INFINITY;"),
     ("resident_bound_off", "if (p < 0 || p >= npages) {", "if (p < 0 || p > npages) {"),
     ("bad_request_kept", "if (req < 0 || req >= P->num_req) {", "if (req < 0) {"),
+    # compressed-K writer
+    ("encode_ties_to_odd", "(d == best_d && (c & 1) == 0 && (best & 1) == 1)",
+     "(d == best_d && (c & 1) == 1 && (best & 1) == 0)"),
+    ("encode_truncates", "if (d < best_d || (d == best_d", "if ((oracle_e4m3((uint8_t)c) <= a && d < best_d) || (d == best_d"),
+    ("encode_sign_dropped", "return (uint8_t)(sign | best);", "return (uint8_t)best;"),
+    ("writer_scale_240", "const float scale = amax / 448.0f;", "const float scale = amax / 240.0f;"),
+    ("writer_scale_big_endian", "rec[OR_D + j] = (uint8_t)(bits >> (8 * j));",
+     "rec[OR_D + j] = (uint8_t)(bits >> (8 * (3 - j)));"),
+    ("writer_record_off_by_one", "memcpy(kv + phys * page_stride + (p % OR_PAGE) * OR_REC_BYTES, rec, OR_REC_BYTES);",
+     "memcpy(kv + phys * page_stride + (p % OR_PAGE + 1) * OR_REC_BYTES, rec, OR_REC_BYTES);"),
+    ("writer_page_table_ignored", "const int64_t phys = page_table[r * pt_stride + p / OR_PAGE];",
+     "const int64_t phys = p / OR_PAGE;"),
+    ("writer_amax_signed", "const float a = fabsf(x[d]);", "const float a = x[d];"),
 ]
 
 
