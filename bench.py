@@ -12,6 +12,9 @@ L2, so no flush is needed between steps.
 Prints one JSON line. `--impl reference` times the fp64 CPU oracle instead
 (the reference arm). Under torchrun each rank scores its own batch (seed =
 rank): weak scaling, no collective on the data path.
+
+`--op write_keys` measures the compressed-K writer instead: one step rewrites
+every record of the workload's cache from bf16 key rows resident in HBM.
 """
 from __future__ import annotations
 
@@ -385,6 +388,93 @@ def run_native(args):
     return 0
 
 
+def run_write_keys(args):
+    """The compressed-K writer on the workload's cache geometry: every visible
+    record of every request rewritten from bf16 rows (one row per record)."""
+    import torch
+    from sparse_attention_kv_e4m3_gb300 import build, native, synth
+
+    build.build()
+    native.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = synth.config(args.workload)
+    lens = [int(x) for x in w.q_len]
+    req = np.concatenate([np.full(L, r, np.int32) for r, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    n = int(req.size)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    keys = torch.randn((n, 128), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    req_d, pos_d = torch.from_numpy(req).to(dev), torch.from_numpy(pos).to(dev)
+    pt_d = torch.from_numpy(np.ascontiguousarray(w.page_table, dtype=np.int32)).to(dev)
+    kv = torch.zeros(w.kv.shape, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    del w
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        native.csa_index_write_keys(keys, pos_d, kv, pt_d, row_req=req_d, dev_status=status, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except Exception:
+        pass
+    sampler = ClockSampler(bus)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = min(args.steps, 200)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    extra = 0
+    while time.perf_counter() - t_wall < 1.2:
+        step()
+        extra += 1
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if extra:
+        clocks["window"] = f"timed region ({wall:.3f} s) plus {extra} identical untimed steps"
+    ms = e0.elapsed_time(e1) / steps
+    # algorithmic bytes per row: the bf16 row, its request and position, one
+    # page-table entry, and the 132-byte record written
+    alg = n * (256 + 4 + 4 + 4 + 132)
+    peak, src = measured_peaks()
+    gbs = alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "compressed-K writer rows/s and HBM GB/s (fraction of peak)",
+        "value": n / (ms * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": 1,
+        "steps": steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "dtype": "bf16->e4m3",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} cache rewritten", "rows": n,
+                   "l2": "inputs and cache larger than L2; no flush"},
+        "roofline": {"kernel": "write_keys_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
+                     "peak_source": f"{src} hbm_gbs", "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": alg},
+        "clocks": clocks,
+        "gpu_launches": steps,
+        "device_status": int(status.item()),
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,7 +483,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="long_ragged_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="index", choices=["index", "write_keys"])
     args = ap.parse_args()
+    if args.op == "write_keys":
+        return run_write_keys(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_native(args)

@@ -222,6 +222,61 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
 csa_status csa_index_score_topk_fused_static(const csa_index_args* args, int32_t k, int32_t* idx, float* vals,
                                              void* stream);
 
+/* Element type of the key rows given to csa_index_write_keys. */
+enum { CSA_KEYS_F32 = 0, CSA_KEYS_BF16 = 1 };
+
+/*
+ * Rows for csa_index_write_keys, the compressed-K writer: the step before the
+ * indexer path that stores new keys in the cache's record format (the BatchGen
+ * #153 commit log's store kernel for the "[128B fp8 | 4B fp32 scale]" layout of
+ * FlashMemory-DeepSeek-V4, "compressed_k format").
+ *
+ * keys       [n, 128] of key_dtype (CSA_KEYS_F32 or CSA_KEYS_BF16), contiguous, 16-byte
+ *            aligned.
+ * row_req    [n] int32 request of each row, or NULL for row i -> request i.
+ * row_pos    [n] int32 logical record position of each row in its request's history.
+ * kv, num_pages, page_stride_bytes, page_table, num_req, pt_stride: the cache, as in
+ *            csa_index_args; kv is written.
+ * dev_status optional int32 in device memory for CSA_DEV_* bits.
+ */
+typedef struct csa_write_args {
+  const void* keys;
+  int32_t key_dtype;
+  int32_t reserved0;         /* must be 0 */
+  int64_t n;
+  const int32_t* row_req;
+  const int32_t* row_pos;
+  uint8_t* kv;
+  int64_t num_pages;
+  int64_t page_stride_bytes;
+  const int32_t* page_table;
+  int32_t num_req;
+  int32_t pt_stride;
+  int32_t* dev_status;
+} csa_write_args;
+
+/*
+ * Quantises each key row x and stores it as the record at page_table[req][pos / 64],
+ * row pos % 64 of that page:
+ *   amax   = max_d |x_d|
+ *   scale  = amax / 448                            (binary32, round to nearest even)
+ *   code_d = e4m3(x_d / scale)                     (x_d / scale in binary32; the nearest
+ *            e4m3 value, ties to the even mantissa; magnitudes past 448 saturate)
+ * A row whose scale is 0 (amax == 0, or amax / 448 underflows in binary32) is stored
+ * as 128 zero codes and scale 0. Record bytes: the
+ * 128 codes, then the scale little-endian. Only the targeted records are written;
+ * rows must target distinct records (otherwise one of them wins).
+ * Device errors (that row is not written; checked in this order, one bit per row):
+ * request outside [0, num_req) CSA_DEV_BAD_REQUEST; position outside [0, 64*pt_stride)
+ * CSA_DEV_LEN_OOB; physical page outside [0, num_pages) CSA_DEV_PAGE_OOB; a non-finite
+ * value CSA_DEV_RANGE.
+ * Host errors: CSA_ERR_INVALID_ARG (null pointers, n < 0, unknown key_dtype, reserved0
+ * != 0, num_req or pt_stride < 1, page_stride_bytes < 64*132 or not a multiple of 16,
+ * num_pages < 1), CSA_ERR_ALIGNMENT (keys, kv or row arrays misaligned), CSA_ERR_CUDA.
+ * n == 0 launches nothing and returns CSA_OK.
+ */
+csa_status csa_index_write_keys(const csa_write_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -89,8 +89,32 @@ def load(path: Optional[str] = None):
             lib.csa_index_score_topk_fused.restype = ctypes.c_int
             lib.csa_index_score_topk_fused_marked.argtypes = [A, i32, vp, vp, vp, sz, vp, vp]
             lib.csa_index_score_topk_fused_marked.restype = ctypes.c_int
+            lib.csa_index_write_keys.argtypes = [ctypes.POINTER(WriteArgs), vp]
+            lib.csa_index_write_keys.restype = ctypes.c_int
             _lib = lib
     return _lib
+
+
+KEYS_F32, KEYS_BF16 = 0, 1
+
+
+class WriteArgs(ctypes.Structure):
+    """Mirror of csa_write_args."""
+    _fields_ = [
+        ("keys", ctypes.c_void_p),
+        ("key_dtype", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("n", ctypes.c_int64),
+        ("row_req", ctypes.c_void_p),
+        ("row_pos", ctypes.c_void_p),
+        ("kv", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int64),
+        ("page_stride_bytes", ctypes.c_int64),
+        ("page_table", ctypes.c_void_p),
+        ("num_req", ctypes.c_int32),
+        ("pt_stride", ctypes.c_int32),
+        ("dev_status", ctypes.c_void_p),
+    ]
 
 
 def status_str(status: int) -> str:
@@ -246,3 +270,26 @@ def csa_index_topk(scores: torch.Tensor, problem: Problem, k: int = 512, ws: Opt
                                vals.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "csa_index_topk")
     return idx, vals
+
+
+def csa_index_write_keys(keys: torch.Tensor, row_pos: torch.Tensor, kv: torch.Tensor, page_table: torch.Tensor,
+                         row_req: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """Compressed-K writer: quantises key rows `keys` [n, 128] (fp32 or bf16) into
+    records of the paged cache `kv` [num_pages, page_stride] (uint8), row i at
+    logical position row_pos[i] of request row_req[i] (identity when None), through
+    `page_table` [num_req, pt_stride]. Every tensor is on the GPU."""
+    if keys.dtype == torch.float32:
+        dt = KEYS_F32
+    elif keys.dtype == torch.bfloat16:
+        dt = KEYS_BF16
+    else:
+        raise TypeError("keys must be float32 or bfloat16")
+    assert keys.dim() == 2 and keys.shape[1] == HEAD_DIM and keys.is_contiguous()
+    assert kv.dtype == torch.uint8 and kv.dim() == 2 and kv.is_contiguous()
+    assert row_pos.dtype == torch.int32 and page_table.dtype == torch.int32
+    pt = page_table.contiguous()
+    a = WriteArgs(keys.data_ptr(), dt, 0, int(keys.shape[0]), _ptr(row_req), row_pos.data_ptr(), kv.data_ptr(),
+                  int(kv.shape[0]), int(kv.shape[1]), pt.data_ptr(), int(pt.shape[0]), int(pt.shape[1]),
+                  _ptr(dev_status))
+    _check(load().csa_index_write_keys(ctypes.byref(a), _stream(stream)), "csa_index_write_keys")

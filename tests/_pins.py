@@ -421,9 +421,14 @@ def pin_writer_matches_generator(o: O.Oracle):
 
 
 def pin_writer_closed_forms(o: O.Oracle):
-    # zero row: zero codes and zero scale
+    # zero row, and a row whose scale amax / 448 underflows: zero codes and zero scale
     rec, _ = o.quantise_row(np.zeros(D, np.float32))
     assert not rec.any()
+    tiny = np.zeros(D, np.float32)
+    tiny[[3, 40]] = np.array([1e-44, -3e-45], np.float32)  # subnormal; 1e-44 / 448 rounds to 0
+    rec, _ = o.quantise_row(tiny)
+    assert not rec.any()
+    assert o.e4m3_encode(np.array([np.inf, -np.inf, 1e30], np.float32)).tolist() == [0x7E, 0xFE, 0x7E]
     # a row on the e4m3 grid whose largest magnitude is 448: scale 1, exact codes
     codes = np.random.default_rng(3).integers(0, 126, D).astype(np.uint8)
     codes[7] = 0x7E

@@ -127,3 +127,43 @@ def test_empty_batch_is_a_no_op(lib):
     a = _fake_args(num_q=0)
     assert lib.csa_index_score(ctypes.byref(a), None, 0, None) == 0
     assert lib.csa_index_score_topk_fused(ctypes.byref(a), 512, None, None, None, 0, None) == 0
+
+
+def test_write_args_layout_matches_header(tmp_path):
+    fields = [f[0] for f in native.WriteArgs._fields_]
+    src = tmp_path / "wlayout.c"
+    body = "".join(f'printf("{f} %zu\\n", offsetof(csa_write_args, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "csa_index.h"\n'
+                   'int main(void){' + body + 'printf("sizeof %zu\\n", sizeof(csa_write_args));return 0;}\n')
+    exe = tmp_path / "wlayout"
+    subprocess.run(["gcc", "-std=c11", f"-I{build.INCLUDE}", "-o", str(exe), str(src)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    for f in fields:
+        assert int(got[f]) == getattr(native.WriteArgs, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(native.WriteArgs)
+
+
+def _fake_write_args(**kw):
+    """Host-side writer args with aligned fake device addresses: validation only."""
+    a = native.WriteArgs(0x10000, native.KEYS_F32, 0, 4, 0, 0x20000, 0x30000, 8, native.PAGE_BYTES, 0x40000, 2, 4, 0)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("change,want", [
+    (dict(keys=0), 1), (dict(row_pos=0), 1), (dict(kv=0), 1), (dict(page_table=0), 1),
+    (dict(n=-1), 1), (dict(key_dtype=7), 1), (dict(reserved0=1), 1), (dict(num_req=0), 1),
+    (dict(pt_stride=0), 1), (dict(num_pages=0), 1), (dict(page_stride_bytes=native.PAGE_BYTES - 16), 1),
+    (dict(page_stride_bytes=native.PAGE_BYTES + 4), 1),
+    (dict(keys=0x10004), 3), (dict(kv=0x30008), 3), (dict(row_pos=0x20002), 3), (dict(row_req=0x50001), 3),
+])
+def test_write_keys_rejects_bad_args(lib, change, want):
+    st = lib.csa_index_write_keys(ctypes.byref(_fake_write_args(**change)), None)
+    assert st == want, native.status_str(st)
+
+
+def test_write_keys_empty_is_a_no_op(lib):
+    assert lib.csa_index_write_keys(ctypes.byref(_fake_write_args(n=0)), None) == 0
+    assert lib.csa_index_write_keys(None, None) == 1

@@ -49,6 +49,7 @@ MUTATIONS = [
     ("writer_page_table_ignored", "const int64_t phys = page_table[r * pt_stride + p / OR_PAGE];",
      "const int64_t phys = p / OR_PAGE;"),
     ("writer_amax_signed", "const float a = fabsf(x[d]);", "const float a = x[d];"),
+    ("writer_scale_underflow_kept", "    if (scale == 0.0f) {", "    if (amax == 0.0f) {"),
 ]
 
 
