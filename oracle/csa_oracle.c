@@ -368,18 +368,20 @@ int32_t oracle_threads(void) {
  *   c_d   = e4m3(x_d / scale)                (x_d / scale in binary32, then the
  *                                            nearest e4m3 value, ties to the even
  *                                            mantissa; magnitudes past 448 saturate)
- *   a row with amax == 0 is stored as zero codes and scale 0.
+ *   a row whose scale is 0 (amax == 0, or amax so small that amax / 448
+ *   underflows) is stored as zero codes and scale 0.
  * The code is decided in binary32, the precision of the pages' torch cast.
  */
 
 /* binary32 -> OCP E4M3 "fn" byte: the nearest of the 127 non-negative finite
  * e4m3 values (searched one by one), ties to the even mantissa, with the sign of
- * the input. Values beyond 448 get 448 (the largest value is the nearest). NaN
+ * the input. Values beyond 448, infinities included, get 448 (saturation). NaN
  * gives the NaN code 0x7F. */
 uint8_t oracle_e4m3_encode(float v) {
   if (isnan(v)) return 0x7F;
   const uint8_t sign = signbit(v) ? 0x80 : 0x00;
   const double a = fabs((double)v);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);  /* the largest value is the nearest (infinities too) */
   int best = 0;
   double best_d = a;  /* distance to code 0 (value 0) */
   for (int c = 1; c < 127; ++c) {
@@ -407,7 +409,7 @@ int32_t oracle_quantise_row(const float* x, uint8_t* rec) {
   }
   const float scale = amax / 448.0f;
   for (int d = 0; d < OR_D; ++d) {
-    if (amax == 0.0f) {
+    if (scale == 0.0f) {
       rec[d] = 0;
     } else {
       const float y = x[d] / scale;
