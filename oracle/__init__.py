@@ -104,6 +104,10 @@ def _bind(path: str):
                                       ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int32]
     lib.oracle_write_keys.restype = ctypes.c_int32
+    lib.oracle_recall.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int64,
+                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_int32, ctypes.c_void_p]
+    lib.oracle_recall.restype = ctypes.c_int32
     return lib
 
 
@@ -202,6 +206,9 @@ class Oracle:
 
     def write_keys(self, keys, req, pos, kv, page_table) -> int:
         return _write_keys(self.lib, keys, req, pos, kv, page_table)
+
+    def recall(self, layers, mean: bool, threshold: float, sink: int, recent: int):
+        return _recall(self.lib, layers, mean, threshold, sink, recent)
 
 
 def load_build(path: str) -> Oracle:
@@ -340,3 +347,25 @@ def quantise_row(x):
 
 def write_keys(keys, req, pos, kv, page_table) -> int:
     return _write_keys(_load(), keys, req, pos, kv, page_table)
+
+
+def _recall(lib, layers, mean: bool, threshold: float, sink: int, recent: int):
+    """Level-1 recall over `layers` (a list of Problem, one per target layer).
+    Returns (keep uint8 [num_q, stride], scores float64, pages list of arrays, flags)
+    with stride = 64 * pt_stride."""
+    n = len(layers)
+    arr = (_Problem * n)(*[p._s for p in layers])
+    num_q = layers[0].num_q
+    stride = 64 * layers[0].pt_stride
+    keep = np.zeros((num_q, stride), dtype=np.uint8)
+    sc = np.zeros((num_q, stride), dtype=np.float64)
+    ps = max(1, layers[0].pt_stride)
+    pages = np.zeros((num_q, ps), dtype=np.int32)
+    npg = np.zeros(num_q, dtype=np.int32)
+    flags = lib.oracle_recall(ctypes.addressof(arr), n, 1 if mean else 0, float(threshold), int(sink), int(recent),
+                              keep.ctypes.data, stride, sc.ctypes.data, pages.ctypes.data, ps, npg.ctypes.data)
+    return keep, sc, [pages[b, :npg[b]].copy() for b in range(num_q)], int(flags)
+
+
+def recall(layers, mean: bool, threshold: float, sink: int, recent: int):
+    return _recall(_load(), layers, mean, threshold, sink, recent)

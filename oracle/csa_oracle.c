@@ -460,3 +460,63 @@ int32_t oracle_write_keys(const float* keys, int64_t n, const int32_t* req, cons
   }
   return flags;
 }
+
+/* ------------------------------------------------------------------ Level-1 recall
+ *
+ * FlashMemory-DeepSeek-V4, "Two-level recall algorithm", Level 1, and "Joint
+ * checkpoint + ensemble": the Memory Indexer scores the full history of each
+ * query row at the target layers (each with its own 128-head query, weights
+ * and compressed keys), the per-layer sigmoid scores are ensembled per chunk
+ * (max, the default "union", or mean), and the resident set is the chunks whose
+ * ensemble score reaches the threshold plus the recency tail and the attention
+ * sink ("threshold + recent + sink"). The pages print neither the threshold nor
+ * the tail and sink sizes: they are parameters here.
+ *
+ * keep [num_q, keep_stride]: 1 / 0 for positions below the row's visible
+ * length; scores: the ensemble scores there (fp64). pages [num_q, pages_stride]:
+ * the logical pages holding a resident chunk, ascending; n_pages their count.
+ * The layers share num_q, q_req, q_len and pt_stride (not checked here).
+ */
+int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t ensemble_mean, double threshold,
+                      int64_t sink, int64_t recent, uint8_t* keep, int64_t keep_stride, double* scores,
+                      int32_t* pages, int32_t pages_stride, int32_t* n_pages) {
+  const int32_t num_q = layers[0].num_q;
+  const int64_t cells = (int64_t)num_q * keep_stride;
+  double* logit = (double*)malloc(sizeof(double) * (cells > 0 ? cells : 1));
+  double* acc = (double*)calloc(cells > 0 ? cells : 1, sizeof(double));
+  int32_t flags = 0;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    flags |= oracle_logits(&layers[l], logit, NULL, keep_stride);
+    for (int32_t b = 0; b < num_q; ++b) {
+      const int64_t L = oracle_visible(&layers[l], b, NULL, NULL, NULL);
+      for (int64_t n = 0; n < L; ++n) {
+        const double sc = oracle_sigmoid(logit[(int64_t)b * keep_stride + n]);
+        double* a = &acc[(int64_t)b * keep_stride + n];
+        if (l == 0)
+          *a = sc;
+        else
+          *a = ensemble_mean ? *a + sc : (sc > *a ? sc : *a);
+      }
+    }
+  }
+  for (int32_t b = 0; b < num_q; ++b) {
+    const int64_t L = oracle_visible(&layers[0], b, NULL, NULL, NULL);
+    int32_t listed = 0;
+    int64_t last_page = -1;
+    for (int64_t n = 0; n < L; ++n) {
+      const int64_t o = (int64_t)b * keep_stride + n;
+      const double e = ensemble_mean ? acc[o] / n_layers : acc[o];
+      const int k = e >= threshold || n < sink || n >= L - recent;
+      keep[o] = (uint8_t)k;
+      if (scores) scores[o] = e;
+      if (k && n / OR_PAGE != last_page) {
+        last_page = n / OR_PAGE;
+        pages[(int64_t)b * pages_stride + listed++] = (int32_t)last_page;
+      }
+    }
+    n_pages[b] = listed;
+  }
+  free(logit);
+  free(acc);
+  return flags;
+}

@@ -487,4 +487,99 @@ def pin_writer_geometry(o: O.Oracle):
     assert np.array_equal(kv2, want)
 
 
+# ---------------------------------------------------------------- Level-1 recall
+
+H1 = 128  # heads of the Memory Indexer's query
+
+
+def recall_layers(n_layers: int, num_q: int, history, seed: int, zero_weights=()):
+    """Target layers of a Level-1 problem: one generated cache per layer (same
+    lengths, its own keys and page table) with a 128-head bf16 query and weights
+    N(0,1) * 128^-0.5 * 128^-0.5."""
+    layers = []
+    for l in range(n_layers):
+        w = synth.make_workload(f"l1_{l}", num_q=num_q, history=list(history), seed=seed + 17 * l, threads=1)
+        rng = np.random.default_rng(seed + 101 * l)
+        w.q = bf16_bits(rng.standard_normal((num_q, H1, D))).reshape(num_q, H1, D)
+        w.fused_w = (rng.standard_normal((num_q, H1)) / np.sqrt(D) / np.sqrt(H1)).astype(np.float32)
+        if l in zero_weights:
+            w.fused_w[:] = 0.0
+        layers.append(w)
+    return layers
+
+
+def _kept_tail_and_sink(L: int, sink: int, recent: int) -> np.ndarray:
+    n = np.arange(L)
+    return ((n < sink) | (n >= L - recent)).astype(np.uint8)
+
+
+def pin_recall_zero_weights(o: O.Oracle):
+    """With every weight 0 each layer scores 0.5 everywhere: a threshold of 0.5
+    keeps every chunk, one just above keeps exactly the sink and the tail."""
+    layers = recall_layers(2, 2, [200, 70], seed=31, zero_weights=(0, 1))
+    P = [O.Problem(w) for w in layers]
+    for mean in (False, True):
+        keep, sc, pages, _ = o.recall(P, mean, 0.5, 3, 70)
+        for b, L in enumerate((200, 70)):
+            assert np.all(sc[b, :L] == 0.5) and np.all(keep[b, :L] == 1)
+            assert list(pages[b]) == list(range((L + PAGE - 1) // PAGE))
+        keep, sc, pages, _ = o.recall(P, mean, 0.5000001, 3, 70)
+        assert np.array_equal(keep[0, :200], _kept_tail_and_sink(200, 3, 70))
+        assert list(pages[0]) == [0, 2, 3]   # n < 3 and 130 <= n < 200
+        assert np.all(keep[1, :70] == 1)   # the tail covers the whole row
+    keep, sc, pages, _ = o.recall(P, False, 2.0, 0, 0)
+    assert not keep[0, :200].any() and len(pages[0]) == 0
+
+
+def pin_recall_matches_brute_force(o: O.Oracle):
+    """Per-layer 128-head logits of an independent numpy restatement, sigmoid,
+    then max or mean across three layers; the keep rule at the median score."""
+    layers = recall_layers(3, 2, [130, 77], seed=32)
+    brute = [brute_logits(w) for w in layers]
+    P = [O.Problem(w) for w in layers]
+    for mean in (False, True):
+        want = {}
+        for key in brute[0]:
+            s = [1.0 / (1.0 + math.exp(-bl[key][0])) for bl in brute]
+            want[key] = sum(s) / len(s) if mean else max(s)
+        v = np.sort(np.array(list(want.values())))
+        m = len(v) // 2
+        while v[m + 1] - v[m] < 1e-9:  # a threshold between two scores, not on one
+            m += 1
+        thr = float((v[m] + v[m + 1]) / 2)
+        keep, sc, pages, _ = o.recall(P, mean, thr, 2, 5)
+        for (b, pos), e in want.items():
+            assert abs(sc[b, pos] - e) <= 1e-12, (b, pos)
+            L = int(layers[0].q_len[b])
+            assert keep[b, pos] == int(e >= thr or pos < 2 or pos >= L - 5), (b, pos)
+        for b in range(2):
+            L = int(layers[0].q_len[b])
+            kept_pages = sorted({p // PAGE for p in range(L) if keep[b, p]})
+            assert list(pages[b]) == kept_pages
+
+
+def pin_recall_ensemble_closed_form(o: O.Oracle):
+    """Layer A has zero weights (0.5 everywhere); layer B a one-hot query on one
+    head: its score is sigmoid(max(0, s * e4m3(byte[d0])) * w). Max and mean of the
+    two follow in closed form."""
+    layers = recall_layers(2, 1, [64], seed=33, zero_weights=(0,))
+    wB = layers[1]
+    q = np.zeros((1, H1, D), np.float32)
+    q[0, 5, 9] = 1.0
+    wB.q = bf16_bits(q).reshape(1, H1, D)
+    wB.fused_w[:] = 0.0
+    wB.fused_w[0, 5] = 0.75
+    P = [O.Problem(w) for w in layers]
+    phys = int(wB.page_table[0, 0])
+    for mean in (False, True):
+        _, sc, _, _ = o.recall(P, mean, 0.9, 0, 0)
+        for r in range(PAGE):
+            rec = wB.kv[phys, r * REC:(r + 1) * REC]
+            s = struct.unpack("<f", rec[D:].tobytes())[0]
+            x = float(torch.tensor([int(rec[9])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item())
+            sB = 1.0 / (1.0 + math.exp(-max(0.0, s * x) * 0.75))
+            want = (0.5 + sB) / 2 if mean else max(0.5, sB)
+            assert abs(sc[0, r] - want) <= 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

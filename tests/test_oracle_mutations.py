@@ -50,6 +50,19 @@ MUTATIONS = [
      "const int64_t phys = p / OR_PAGE;"),
     ("writer_amax_signed", "const float a = fabsf(x[d]);", "const float a = x[d];"),
     ("writer_scale_underflow_kept", "    if (scale == 0.0f) {", "    if (amax == 0.0f) {"),
+    # Level-1 recall
+    ("recall_max_is_min", "*a = ensemble_mean ? *a + sc : (sc > *a ? sc : *a);",
+     "*a = ensemble_mean ? *a + sc : (sc < *a ? sc : *a);"),
+    ("recall_mean_not_divided", "const double e = ensemble_mean ? acc[o] / n_layers : acc[o];",
+     "const double e = acc[o];"),
+    ("recall_threshold_strict", "const int k = e >= threshold || n < sink || n >= L - recent;",
+     "const int k = e > threshold || n < sink || n >= L - recent;"),
+    ("recall_sink_off_by_one", "const int k = e >= threshold || n < sink || n >= L - recent;",
+     "const int k = e >= threshold || n <= sink || n >= L - recent;"),
+    ("recall_tail_off_by_one", "const int k = e >= threshold || n < sink || n >= L - recent;",
+     "const int k = e >= threshold || n < sink || n > L - recent;"),
+    ("recall_sigmoid_skipped", "const double sc = oracle_sigmoid(logit[(int64_t)b * keep_stride + n]);",
+     "const double sc = logit[(int64_t)b * keep_stride + n];"),
 ]
 
 
