@@ -475,7 +475,10 @@ int32_t oracle_write_keys(const float* keys, int64_t n, const int32_t* req, cons
  * keep [num_q, keep_stride]: 1 / 0 for positions below the row's visible
  * length; scores: the ensemble scores there (fp64). pages [num_q, pages_stride]:
  * the logical pages holding a resident chunk, ascending; n_pages their count.
- * The layers share num_q, q_req, q_len and pt_stride (not checked here).
+ * The layers share num_q, num_req and pt_stride (not checked here); the rows
+ * (q_len, q_req) are layer 0's in every layer. Reading for invalid geometry
+ * (the pages do not speak of it): a chunk whose page is out of range in a
+ * layer has no score from that layer and counts 0 there; the flag is raised.
  */
 int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t ensemble_mean, double threshold,
                       int64_t sink, int64_t recent, uint8_t* keep, int64_t keep_stride, double* scores,
@@ -483,15 +486,23 @@ int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t en
   const int32_t num_q = layers[0].num_q;
   const int64_t cells = (int64_t)num_q * keep_stride;
   double* logit = (double*)malloc(sizeof(double) * (cells > 0 ? cells : 1));
+  uint8_t* valid = (uint8_t*)malloc(cells > 0 ? cells : 1);
   double* acc = (double*)calloc(cells > 0 ? cells : 1, sizeof(double));
+  int64_t* len = (int64_t*)calloc(num_q > 0 ? num_q : 1, sizeof(int64_t));
   int32_t flags = 0;
+  for (int32_t b = 0; b < num_q; ++b)
+    len[b] = row_request(&layers[0], b, &flags) < 0 ? 0 : row_length(&layers[0], b, &flags);
   for (int32_t l = 0; l < n_layers; ++l) {
-    flags |= oracle_logits(&layers[l], logit, NULL, keep_stride);
+    oracle_problem P = layers[l];
+    P.q_len = layers[0].q_len;
+    P.q_req = layers[0].q_req;
+    memset(valid, 0, cells > 0 ? cells : 1);
+    flags |= oracle_logits(&P, logit, valid, keep_stride);
     for (int32_t b = 0; b < num_q; ++b) {
-      const int64_t L = oracle_visible(&layers[l], b, NULL, NULL, NULL);
-      for (int64_t n = 0; n < L; ++n) {
-        const double sc = oracle_sigmoid(logit[(int64_t)b * keep_stride + n]);
-        double* a = &acc[(int64_t)b * keep_stride + n];
+      for (int64_t n = 0; n < len[b]; ++n) {
+        const int64_t o = (int64_t)b * keep_stride + n;
+        const double sc = valid[o] ? oracle_sigmoid(logit[o]) : 0.0;
+        double* a = &acc[o];
         if (l == 0)
           *a = sc;
         else
@@ -500,7 +511,7 @@ int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t en
     }
   }
   for (int32_t b = 0; b < num_q; ++b) {
-    const int64_t L = oracle_visible(&layers[0], b, NULL, NULL, NULL);
+    const int64_t L = len[b];
     int32_t listed = 0;
     int64_t last_page = -1;
     for (int64_t n = 0; n < L; ++n) {
@@ -517,6 +528,8 @@ int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t en
     n_pages[b] = listed;
   }
   free(logit);
+  free(valid);
   free(acc);
+  free(len);
   return flags;
 }

@@ -492,13 +492,13 @@ def pin_writer_geometry(o: O.Oracle):
 H1 = 128  # heads of the Memory Indexer's query
 
 
-def recall_layers(n_layers: int, num_q: int, history, seed: int, zero_weights=()):
+def recall_layers(n_layers: int, num_q: int, history, seed: int, zero_weights=(), **kw):
     """Target layers of a Level-1 problem: one generated cache per layer (same
     lengths, its own keys and page table) with a 128-head bf16 query and weights
     N(0,1) * 128^-0.5 * 128^-0.5."""
     layers = []
     for l in range(n_layers):
-        w = synth.make_workload(f"l1_{l}", num_q=num_q, history=list(history), seed=seed + 17 * l, threads=1)
+        w = synth.make_workload(f"l1_{l}", num_q=num_q, history=list(history), seed=seed + 17 * l, threads=1, **kw)
         rng = np.random.default_rng(seed + 101 * l)
         w.q = bf16_bits(rng.standard_normal((num_q, H1, D))).reshape(num_q, H1, D)
         w.fused_w = (rng.standard_normal((num_q, H1)) / np.sqrt(D) / np.sqrt(H1)).astype(np.float32)
@@ -580,6 +580,33 @@ def pin_recall_ensemble_closed_form(o: O.Oracle):
             sB = 1.0 / (1.0 + math.exp(-max(0.0, s * x) * 0.75))
             want = (0.5 + sB) / 2 if mean else max(0.5, sB)
             assert abs(sc[0, r] - want) <= 1e-12
+
+
+def pin_recall_rows_and_unreadable_pages(o: O.Oracle):
+    """Rows come from layer 0 (another layer's q_len is ignored); a chunk on a page
+    that a layer maps out of range scores 0 in that layer; a row with a request id
+    out of range is empty. One layer: a threshold just above 0 keeps every readable
+    chunk and no unreadable one outside the tail. Two layers, mean: the chunks of
+    the unreadable page score half of the other layer's score."""
+    layers = recall_layers(2, 3, [300, 300, 300], seed=34)
+    layers[1].page_table = layers[1].page_table.copy()
+    layers[1].page_table[0, 2] = layers[1].num_pages + 1   # row 0, positions 128..191
+    keep1, sc1, pages1, f1 = o.recall([O.Problem(layers[1])], False, 1e-300, 0, 10)
+    assert f1 & O.PAGE_OOB
+    assert np.all(sc1[0, 128:192] == 0.0) and np.all(keep1[0, 128:192] == 0)
+    assert np.all(keep1[0, :128] == 1) and np.all(keep1[0, 192:300] == 1)
+    assert list(pages1[0]) == [0, 1, 3, 4]
+    layers[1].q_len = np.array([5, 5, 5], np.int32)  # ignored: layer 0's rows rule
+    layers[0].q_req = np.array([0, 1, 7], np.int32)  # row 2: request out of range
+    layers[1].q_req = np.array([0, 1, 2], np.int32)  # ignored too
+    P = [O.Problem(w) for w in layers]
+    keep, sc, pages, flags = o.recall(P, True, 2.0, 0, 0)
+    assert flags & O.PAGE_OOB and flags & O.BAD_REQUEST
+    _, sc0, _, _ = o.recall([P[0]], False, 2.0, 0, 0)
+    assert np.all(sc[0, 128:192] == sc0[0, 128:192] / 2)
+    assert np.all(sc[0, :128] > sc0[0, :128] / 2)   # both layers score there
+    assert sc[1, 299] > 0.0                          # layer 1's q_len of 5 is not used
+    assert not keep[2].any() and len(pages[2]) == 0 and np.all(sc[2] == 0.0)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

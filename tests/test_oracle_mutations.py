@@ -61,8 +61,11 @@ MUTATIONS = [
      "const int k = e >= threshold || n <= sink || n >= L - recent;"),
     ("recall_tail_off_by_one", "const int k = e >= threshold || n < sink || n >= L - recent;",
      "const int k = e >= threshold || n < sink || n > L - recent;"),
-    ("recall_sigmoid_skipped", "const double sc = oracle_sigmoid(logit[(int64_t)b * keep_stride + n]);",
-     "const double sc = logit[(int64_t)b * keep_stride + n];"),
+    ("recall_sigmoid_skipped", "const double sc = valid[o] ? oracle_sigmoid(logit[o]) : 0.0;",
+     "const double sc = valid[o] ? logit[o] : 0.0;"),
+    ("recall_unreadable_scores_half", "const double sc = valid[o] ? oracle_sigmoid(logit[o]) : 0.0;",
+     "const double sc = valid[o] ? oracle_sigmoid(logit[o]) : 0.5;"),
+    ("recall_rows_of_each_layer", "    P.q_len = layers[0].q_len;\n    P.q_req = layers[0].q_req;\n", ""),
 ]
 
 
