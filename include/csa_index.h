@@ -158,6 +158,13 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
                            void* stream);
 
 /*
+ * csa_index_score writing the logits themselves (sum_h relu(k . q_h) * fused_w_h, before
+ * the sigmoid), in the same layout, with the same arguments and errors. For callers that
+ * combine several scorers before the sigmoid (two halves of a 128-head query).
+ */
+csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t stride, void* stream);
+
+/*
  * Top-k over a caller-provided score matrix laid out as csa_index_score writes it
  * (the "Top-k Selector" of "Two-level recall algorithm", Level 2). Only the bounds
  * fields of `args` are read: num_q, num_req, q_req, q_len, resident, n_resident,
@@ -221,6 +228,63 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
  */
 csa_status csa_index_score_topk_fused_static(const csa_index_args* args, int32_t k, int32_t* idx, float* vals,
                                              void* stream);
+
+/* Ensemble of the per-layer scores in csa_recall_level1. */
+enum { CSA_ENSEMBLE_MAX = 0, CSA_ENSEMBLE_MEAN = 1 };
+
+/*
+ * Level-1 recall (FlashMemory-DeepSeek-V4, "Two-level recall algorithm", Level 1, and
+ * "Joint checkpoint + ensemble"): the Memory Indexer scores the full history of each query
+ * row at n_layers target layers (l10, l12 and l20 on the pages) with 128-head queries
+ * (the retriever's --n-heads 128); the per-layer sigmoid scores are combined per chunk,
+ * by max (the pages' default, "union") or mean; a chunk is resident when the combined
+ * score reaches `threshold` or it is one of the row's first `sink` or last `recent`
+ * chunks ("threshold + recent + sink"). The pages print neither the threshold nor the two
+ * counts: they are parameters.
+ *
+ * layers       host array of n_layers csa_index_args, one per layer: q [num_q, 128, 128]
+ *              bf16 and fused_w [num_q, 128] of that layer's retriever, and that layer's
+ *              compressed-K cache (kv, num_pages, page_stride_bytes, page_table, num_req,
+ *              pt_stride). num_heads must be 128; num_q, num_req and pt_stride must be the
+ *              same in every layer; the rows (q_len, q_req) are layer 0's in every layer
+ *              (the other layers' q_len and q_req are not read); resident must be NULL
+ *              (Level 1 reads the whole history). dev_status of layer 0 receives the
+ *              device error bits of every layer.
+ * ensemble     CSA_ENSEMBLE_MAX or CSA_ENSEMBLE_MEAN.
+ * keep         [num_q, keep_stride] uint8 out: 1 for a resident chunk, else 0, at positions
+ *              below the row's visible length (others are not written);
+ *              keep_stride >= 64 * pt_stride.
+ * pages        [num_q, pages_stride] int32 out: the logical pages that hold at least one
+ *              resident chunk, ascending; n_pages [num_q] their count. For decode (q_req
+ *              NULL) these are the Level-2 resident lists (csa_index_args.resident,
+ *              n_resident with res_stride = pages_stride). pages_stride >= pt_stride.
+ * scores       optional [num_q, keep_stride] fp32 out: the combined scores (written where
+ *              keep is).
+ * Errors: as csa_index_score for each layer, plus CSA_ERR_INVALID_ARG for n_layers outside
+ * [1, 8], an unknown ensemble, a NaN threshold, negative sink or recent, strides too small,
+ * layers that disagree on num_q, num_req or pt_stride, or a resident list given; and
+ * CSA_ERR_WORKSPACE when ws is smaller than csa_recall_workspace_bytes.
+ */
+typedef struct csa_recall_args {
+  const csa_index_args* layers;
+  int32_t n_layers;
+  int32_t ensemble;
+  float threshold;
+  int32_t sink;
+  int32_t recent;
+  int32_t pages_stride;
+  uint8_t* keep;
+  int64_t keep_stride;
+  int32_t* pages;
+  int32_t* n_pages;
+  float* scores;
+} csa_recall_args;
+
+/* Device workspace csa_recall_level1 needs for these arguments (host arithmetic only);
+ * 0 when num_q < 0 or keep_stride < 0. */
+size_t csa_recall_workspace_bytes(const csa_recall_args* args);
+
+csa_status csa_recall_level1(const csa_recall_args* args, void* ws, size_t ws_bytes, void* stream);
 
 /* Element type of the key rows given to csa_index_write_keys. */
 enum { CSA_KEYS_F32 = 0, CSA_KEYS_BF16 = 1 };

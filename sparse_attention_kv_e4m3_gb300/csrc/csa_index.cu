@@ -134,6 +134,7 @@ struct Params {
   int32_t res_stride;
   int32_t k;
   int32_t grid;         // CTAs of the phase-1 kernel (slot numbering)
+  int32_t raw_logits;   // score mode: write the logit instead of its sigmoid
 };
 
 struct PageInfo {
@@ -702,7 +703,8 @@ __device__ void role_worker(const Params& P, Smem& S) {
       float* out = P.scores + static_cast<int64_t>(b) * P.score_stride + lt * kTile + row;
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
-        if (!isnan(__uint_as_float(sc[sub]))) out[kMmaRows * sub] = __frcp_rn(1.0f + __expf(-logit[sub]));
+        if (!isnan(__uint_as_float(sc[sub])))
+          out[kMmaRows * sub] = P.raw_logits ? logit[sub] : __frcp_rn(1.0f + __expf(-logit[sub]));
     } else {
       const int slot = static_cast<int>(i % kKeyRing);
       const bool ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
@@ -1261,6 +1263,24 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
   P.scores = scores;
   P.score_stride = score_stride;
   P.grid = sms;
+  score_kernel<false><<<sms, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(P);
+  return launch_status();
+}
+
+csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t stride, void* stream) {
+  csa_status st = check_args(args, kNeedQ | kNeedKv);
+  if (st != CSA_OK) return st;
+  if (args->num_q == 0) return CSA_OK;
+  if (!logits) return CSA_ERR_INVALID_ARG;
+  if (!aligned(logits, 4)) return CSA_ERR_ALIGNMENT;
+  if (stride < min_score_stride(args)) return CSA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != CSA_OK) return st;
+  Params P = params_of(args);
+  P.scores = logits;
+  P.score_stride = stride;
+  P.grid = sms;
+  P.raw_logits = 1;
   score_kernel<false><<<sms, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(P);
   return launch_status();
 }

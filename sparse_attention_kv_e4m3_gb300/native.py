@@ -91,6 +91,12 @@ def load(path: Optional[str] = None):
             lib.csa_index_score_topk_fused_marked.restype = ctypes.c_int
             lib.csa_index_write_keys.argtypes = [ctypes.POINTER(WriteArgs), vp]
             lib.csa_index_write_keys.restype = ctypes.c_int
+            lib.csa_index_logits.argtypes = [A, vp, i64, vp]
+            lib.csa_index_logits.restype = ctypes.c_int
+            lib.csa_recall_workspace_bytes.argtypes = [ctypes.POINTER(RecallArgs)]
+            lib.csa_recall_workspace_bytes.restype = sz
+            lib.csa_recall_level1.argtypes = [ctypes.POINTER(RecallArgs), vp, sz, vp]
+            lib.csa_recall_level1.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -114,6 +120,27 @@ class WriteArgs(ctypes.Structure):
         ("num_req", ctypes.c_int32),
         ("pt_stride", ctypes.c_int32),
         ("dev_status", ctypes.c_void_p),
+    ]
+
+
+ENSEMBLE_MAX, ENSEMBLE_MEAN = 0, 1
+
+
+class RecallArgs(ctypes.Structure):
+    """Mirror of csa_recall_args."""
+    _fields_ = [
+        ("layers", ctypes.c_void_p),
+        ("n_layers", ctypes.c_int32),
+        ("ensemble", ctypes.c_int32),
+        ("threshold", ctypes.c_float),
+        ("sink", ctypes.c_int32),
+        ("recent", ctypes.c_int32),
+        ("pages_stride", ctypes.c_int32),
+        ("keep", ctypes.c_void_p),
+        ("keep_stride", ctypes.c_int64),
+        ("pages", ctypes.c_void_p),
+        ("n_pages", ctypes.c_void_p),
+        ("scores", ctypes.c_void_p),
     ]
 
 
@@ -293,3 +320,46 @@ def csa_index_write_keys(keys: torch.Tensor, row_pos: torch.Tensor, kv: torch.Te
                   int(kv.shape[0]), int(kv.shape[1]), pt.data_ptr(), int(pt.shape[0]), int(pt.shape[1]),
                   _ptr(dev_status))
     _check(load().csa_index_write_keys(ctypes.byref(a), _stream(stream)), "csa_index_write_keys")
+
+
+def csa_index_logits(problem: "Problem", logits: Optional[torch.Tensor] = None, stride=None, stream=None):
+    """csa_index_score writing logits (before the sigmoid). Returns the [num_q, stride] tensor."""
+    a = problem.args()
+    stride = stride or problem.score_stride()
+    if logits is None:
+        logits = torch.full((problem.num_q, stride), float("nan"), dtype=torch.float32, device=problem.q_len.device)
+    _check(load().csa_index_logits(ctypes.byref(a), logits.data_ptr(), int(stride), _stream(stream)),
+           "csa_index_logits")
+    return logits
+
+
+def csa_recall_level1(layers, mean: bool = False, threshold: float = 0.5, sink: int = 0, recent: int = 0,
+                      scores: bool = True, ws: Optional[torch.Tensor] = None, out=None, stream=None):
+    """Level-1 recall over `layers` (one Problem per target layer, 128-head queries).
+    Returns (keep uint8 [num_q, stride], pages int32 [num_q, pt_stride], n_pages int32 [num_q],
+    scores fp32 [num_q, stride] or None), stride = 64 * pt_stride; `out` may hold these four
+    tensors, preallocated (keep and scores with equal row strides)."""
+    args = [p.args() for p in layers]
+    arr = (Args * len(args))(*args)
+    p0 = layers[0]
+    num_q, pts = p0.num_q, int(p0.page_table.shape[1])
+    stride = PAGE_RECORDS * pts
+    dev = p0.q_len.device
+    if out is None:
+        keep = torch.zeros((num_q, stride), dtype=torch.uint8, device=dev)
+        pages = torch.full((num_q, pts), -1, dtype=torch.int32, device=dev)
+        npg = torch.zeros(num_q, dtype=torch.int32, device=dev)
+        sc = torch.full((num_q, stride), float("nan"), dtype=torch.float32, device=dev) if scores else None
+    else:
+        keep, pages, npg, sc = out
+        stride = int(keep.stride(0))
+        assert sc is None or int(sc.stride(0)) == stride
+    ra = RecallArgs(ctypes.addressof(arr), len(args), ENSEMBLE_MEAN if mean else ENSEMBLE_MAX, float(threshold),
+                    int(sink), int(recent), int(pages.stride(0)), keep.data_ptr(), stride, pages.data_ptr(),
+                    npg.data_ptr(), _ptr(sc))
+    need = load().csa_recall_workspace_bytes(ctypes.byref(ra))
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(load().csa_recall_level1(ctypes.byref(ra), ws.data_ptr(), ws.numel(), _stream(stream)),
+           "csa_recall_level1")
+    return keep, pages, npg, sc

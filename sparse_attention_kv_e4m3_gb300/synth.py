@@ -227,6 +227,24 @@ def make_workload(
     )
 
 
+LEVEL1_HEADS = 128
+
+
+def level1_layers(w: Workload, n_layers: int, seed: int) -> list:
+    """Target layers of a Level-1 recall over the history of `w`: each layer draws
+    its own 128-head query and weights, N(0,1) and N(0,1) * 128^-0.5 * 128^-0.5
+    (the distributions of the 64-head indexer inputs above, at 128 heads); the
+    cache bytes, page table and rows of `w` stand in for every layer's cache."""
+    out = []
+    for l in range(n_layers):
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(7, l))))
+        q = rng.standard_normal((w.num_q, LEVEL1_HEADS, HEAD_DIM), dtype=np.float32)
+        fw = (rng.standard_normal((w.num_q, LEVEL1_HEADS)) * HEAD_DIM ** -0.5 * LEVEL1_HEADS ** -0.5)
+        out.append(Workload(name=f"{w.name}_l{l}", q=_bf16_bits(q), fused_w=fw.astype(np.float32), kv=w.kv,
+                            page_table=w.page_table, q_len=w.q_len, q_req=w.q_req, meta=dict(w.meta, layer=l)))
+    return out
+
+
 def _uniform(lo: int, hi: int):
     return lambda rng, n: rng.integers(lo, hi + 1, size=n)
 

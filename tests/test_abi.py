@@ -167,3 +167,46 @@ def test_write_keys_rejects_bad_args(lib, change, want):
 def test_write_keys_empty_is_a_no_op(lib):
     assert lib.csa_index_write_keys(ctypes.byref(_fake_write_args(n=0)), None) == 0
     assert lib.csa_index_write_keys(None, None) == 1
+
+
+def test_recall_args_layout_matches_header(tmp_path):
+    fields = [f[0] for f in native.RecallArgs._fields_]
+    src = tmp_path / "rlayout.c"
+    body = "".join(f'printf("{f} %zu\\n", offsetof(csa_recall_args, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "csa_index.h"\n'
+                   'int main(void){' + body + 'printf("sizeof %zu\\n", sizeof(csa_recall_args));return 0;}\n')
+    exe = tmp_path / "rlayout"
+    subprocess.run(["gcc", "-std=c11", f"-I{build.INCLUDE}", "-o", str(exe), str(src)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    for f in fields:
+        assert int(got[f]) == getattr(native.RecallArgs, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(native.RecallArgs)
+
+
+def test_recall_rejects_bad_args(lib):
+    layer = _fake_args(num_heads=128)
+    arr = (native.Args * 2)(layer, layer)
+    base = dict(layers=ctypes.addressof(arr), n_layers=2, ensemble=0, threshold=0.5, sink=0, recent=0,
+                pages_stride=4, keep=0x60000, keep_stride=256, pages=0x70000, n_pages=0x80000, scores=0)
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return lib.csa_recall_level1(ctypes.byref(native.RecallArgs(**d)), ctypes.c_void_p(0x90000), 1 << 30, None)
+
+    assert call(n_layers=0) == 1 and call(n_layers=9) == 1 and call(ensemble=2) == 1
+    assert call(threshold=float("nan")) == 1 and call(sink=-1) == 1 and call(recent=-2) == 1
+    assert call(keep_stride=255) == 1 and call(pages_stride=3) == 1 and call(keep=0) == 1
+    assert call(pages=0x70002) == 3
+    arr[1].num_heads = 64  # layers must all have 128 heads
+    assert call() == 1
+    arr[1].num_heads = 128
+    arr[1].pt_stride = 5   # and agree on the rows' geometry
+    assert call() == 1
+    arr[1].pt_stride = 4
+    assert call(layers=0) == 1
+    need = lib.csa_recall_workspace_bytes(ctypes.byref(native.RecallArgs(**base)))
+    assert need > 0
+    assert lib.csa_recall_level1(ctypes.byref(native.RecallArgs(**base)), ctypes.c_void_p(0x90000), need - 1,
+                                 None) == 4
