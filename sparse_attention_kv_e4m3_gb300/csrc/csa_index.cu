@@ -654,22 +654,24 @@ __device__ void role_worker(const Params& P, Smem& S) {
     return true;
   };
 
-  // Logit of this lane's record in sub-tile `sub` of D stage td.
-  // Logit of this lane's record in sub-tile `sub` of D stage td.
-  auto logit_of = [&](int td, int sub, uint32_t sc, int seg) -> float {
-    const float s = __uint_as_float(sc);
+  // Logits of this lane's two records (one per sub-tile) in D stage td. Both
+  // sub-tiles are read per TMEM wait, and their sums are independent chains.
+  // relu(s * x) = |s| * relu(sign(s) * x); in practice every record of the warp
+  // has s >= 0 (one vote), and then the sign multiply drops out.
+  static_assert(kSub == 2, "the epilogue reads two sub-tiles at a time");
+  auto logits_of = [&](int td, const uint32_t (&sc)[kSub], int seg, float (&logit)[kSub]) {
     const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
-    // relu(s * x) = |s| * relu(sign(s) * x); in practice every record of the warp
-    // has s >= 0 (one vote), and then the sign multiply drops out.
-    const float sg = s < 0.0f ? -1.0f : 1.0f;
-    const bool all_pos = __all_sync(0xFFFFFFFFu, sg > 0.0f);
-    float acc[8];
+    const float s0 = __uint_as_float(sc[0]), s1 = __uint_as_float(sc[1]);
+    const float g0 = s0 < 0.0f ? -1.0f : 1.0f, g1 = s1 < 0.0f ? -1.0f : 1.0f;
+    const bool all_pos = __all_sync(0xFFFFFFFFu, g0 > 0.0f && g1 > 0.0f);
+    float a0[8], a1[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int j = 0; j < 8; ++j) a0[j] = a1[j] = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < kH; c += 16) {  // heads c .. c+15 of this lane's record
-      uint32_t x[16];
-      tmem_ld16(tmem + d_col(td) + 64 * sub + c + lane_off, x);
+    for (int c = 0; c < kH; c += 16) {  // heads c .. c+15 of both records
+      uint32_t x0[16], x1[16];
+      tmem_ld16(tmem + d_col(td) + c + lane_off, x0);
+      tmem_ld16(tmem + d_col(td) + 64 + c + lane_off, x1);
       tmem_wait_ld();
       float4 w4[4];
 #pragma unroll
@@ -677,13 +679,20 @@ __device__ void role_worker(const Params& P, Smem& S) {
       const float* w = reinterpret_cast<const float*>(w4);
       if (all_pos) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j & 7] = fmaf(fmaxf(__uint_as_float(x[j]), 0.f), w[j], acc[j & 7]);
+        for (int j = 0; j < 16; ++j) {
+          a0[j & 7] = fmaf(fmaxf(__uint_as_float(x0[j]), 0.f), w[j], a0[j & 7]);
+          a1[j & 7] = fmaf(fmaxf(__uint_as_float(x1[j]), 0.f), w[j], a1[j & 7]);
+        }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j & 7] = fmaf(fmaxf(sg * __uint_as_float(x[j]), 0.f), w[j], acc[j & 7]);
+        for (int j = 0; j < 16; ++j) {
+          a0[j & 7] = fmaf(fmaxf(g0 * __uint_as_float(x0[j]), 0.f), w[j], a0[j & 7]);
+          a1[j & 7] = fmaf(fmaxf(g1 * __uint_as_float(x1[j]), 0.f), w[j], a1[j & 7]);
+        }
       }
     }
-    return fabsf(s) * (((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7])));
+    logit[0] = fabsf(s0) * (((a0[0] + a0[4]) + (a0[1] + a0[5])) + ((a0[2] + a0[6]) + (a0[3] + a0[7])));
+    logit[1] = fabsf(s1) * (((a1[0] + a1[4]) + (a1[1] + a1[5])) + ((a1[2] + a1[6]) + (a1[3] + a1[7])));
   };
 
   // Epilogue of own tile i of row b, local tile lt, segment `seg`; the caller
@@ -693,8 +702,7 @@ __device__ void role_worker(const Params& P, Smem& S) {
     const int td = static_cast<int>(i % kDStages);
     tc_fence_after();
     float logit[kSub];
-#pragma unroll
-    for (int sub = 0; sub < kSub; ++sub) logit[sub] = logit_of(td, sub, sc[sub], seg);
+    logits_of(td, sc, seg, logit);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
