@@ -514,17 +514,70 @@ __device__ void role_mma(const Params& P, Smem& S) {
   mbar_wait_drain(smem_u32(&S.drain), 0);
 }
 
+// Per-head power-of-two scale sc (and 1 / sc) mapping the head's largest |q|,
+// m, into (224, 448]; a non-finite m is flagged and treated as 1.
+__device__ __forceinline__ void head_scale(float m, int32_t* flags, float* sc, float* isc) {
+  if (!isfinite(m)) {
+    *flags |= CSA_DEV_RANGE;
+    m = 1.0f;
+  }
+  int E2;
+  const float f = frexpf(m, &E2);
+  int e = (f <= 0.875f) ? 9 - E2 : 8 - E2;
+  e = e < -126 ? -126 : (e > 126 ? 126 : e);
+  *sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+  *isc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+// e4m3 hi and lo terms of two scaled query values (a in the low byte of each):
+// hi = e4m3(x), lo = e4m3(x - hi).
+__device__ __forceinline__ void split_pair(float a, float c, uint32_t* hi2, uint32_t* lo2) {
+  uint16_t h2, l2;
+  uint32_t hf;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h2) : "f"(c), "f"(a));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hf) : "h"(h2));
+  const float ah = __half2float(__ushort_as_half(static_cast<uint16_t>(hf & 0xFFFFu)));
+  const float ch = __half2float(__ushort_as_half(static_cast<uint16_t>(hf >> 16)));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(l2) : "f"(c - ch), "f"(a - ah));
+  *hi2 = h2;
+  *lo2 = l2;
+}
+
+// Byte offset of K-chunk `chunk` (16 bytes) of head h in a 128-byte-swizzled,
+// K-major query buffer (8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t qbuf_offset(int h, int chunk) {
+  return (h >> 3) * 1024 + (h & 7) * 128 + (((chunk ^ (h & 7)) & 7) << 4);
+}
+
 // Splits one bf16 query row into e4m3 hi + lo terms (per-head power-of-two
 // scale so that the largest |q| maps into (224, 448]) in the swizzled layout.
+//
+// The whole row is requested before the loop (the head weights, one per lane
+// and half, the first batch of q, and the rest of q into L2), and each batch's
+// loads are issued before the previous batch is processed: the first query of
+// a CTA is prepared while every CTA's first page copies load HBM, and a loop
+// that waits for memory once per head or per batch took about 11 us there.
 __device__ void prep_query(const Params& P, Smem& S, int32_t b, int qs, int32_t* flags) {
   const int lane = threadIdx.x & 31;
   const uint16_t* qrow = P.q + static_cast<int64_t>(b) * kH * kD;
+  const float* wrow = P.w + static_cast<int64_t>(b) * kH;
   uint8_t* hi = S.qbuf[qs][0];
   uint8_t* lo = S.qbuf[qs][1];
-  for (int h0 = 0; h0 < kH; h0 += 8) {
-    uint2 raw[8];
+  const float w_first = __ldg(wrow + lane), w_second = __ldg(wrow + 32 + lane);  // heads lane, lane + 32
+  {
+    const char* base = reinterpret_cast<const char*>(qrow);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) raw[j] = *reinterpret_cast<const uint2*>(qrow + (h0 + j) * kD + lane * 4);
+    for (int j = 0; j < 4; ++j) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (lane + 32 * j) * 128));
+  }
+  uint2 raw[8], nxt[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) raw[j] = __ldg(reinterpret_cast<const uint2*>(qrow + j * kD + lane * 4));
+#pragma unroll 1
+  for (int h0 = 0; h0 < kH; h0 += 8) {
+    if (h0 + 8 < kH) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) nxt[j] = __ldg(reinterpret_cast<const uint2*>(qrow + (h0 + 8 + j) * kD + lane * 4));
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int h = h0 + j;
@@ -536,46 +589,74 @@ __device__ void prep_query(const Params& P, Smem& S, int32_t b, int qs, int32_t*
       float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      if (!isfinite(m)) {
-        *flags |= CSA_DEV_RANGE;
-        m = 1.0f;
-      }
-      int E2;
-      const float f = frexpf(m, &E2);
-      int e = (f <= 0.875f) ? 9 - E2 : 8 - E2;
-      e = e < -126 ? -126 : (e > 126 ? 126 : e);
-      const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-      const float isc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      float sc, isc;
+      head_scale(m, flags, &sc, &isc);
       uint32_t whi = 0, wlo = 0;
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr) {
-        const float a = x[2 * pr] * sc, c = x[2 * pr + 1] * sc;
-        uint16_t h2, l2;
-        uint32_t hf;
-        // pack: the second operand lands in the low byte
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h2) : "f"(c), "f"(a));
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hf) : "h"(h2));
-        const float ah = __half2float(__ushort_as_half(static_cast<uint16_t>(hf & 0xFFFFu)));
-        const float ch = __half2float(__ushort_as_half(static_cast<uint16_t>(hf >> 16)));
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(l2) : "f"(c - ch), "f"(a - ah));
-        whi |= static_cast<uint32_t>(h2) << (16 * pr);
-        wlo |= static_cast<uint32_t>(l2) << (16 * pr);
+        uint32_t h2, l2;
+        split_pair(x[2 * pr] * sc, x[2 * pr + 1] * sc, &h2, &l2);
+        whi |= h2 << (16 * pr);
+        wlo |= l2 << (16 * pr);
       }
-      const uint32_t off = (h >> 3) * 1024 + (h & 7) * 128 + ((((lane >> 2) ^ (h & 7)) & 7) << 4) + (lane & 3) * 4;
+      const uint32_t off = qbuf_offset(h, lane >> 2) + (lane & 3) * 4;
       *reinterpret_cast<uint32_t*>(hi + off) = whi;
       *reinterpret_cast<uint32_t*>(lo + off) = wlo;
-      if (lane == 0) S.wbuf[qs][h] = P.w[static_cast<int64_t>(b) * kH + h] * isc;
+      if (lane == (h & 31)) S.wbuf[qs][h] = (h < 32 ? w_first : w_second) * isc;
     }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) raw[j] = nxt[j];
   }
 }
 
+// The first segment's query, prepared by the whole CTA in the kernel's prologue,
+// before any page copy is in flight, into query slot 0: thread t takes the 16
+// elements 16p .. 16p+15 of head h = t / 8 (p = t % 8), so that the row's loads
+// are all issued at once. Same arithmetic and layout as prep_query.
+static_assert(kThreads == kH * (kD / 16), "one thread per 16 elements of a query row");
+__device__ void prep_first_query(const Params& P, Smem& S, int32_t b, int32_t* flags) {
+  const int tid = threadIdx.x, h = tid >> 3, p = tid & 7;
+  const uint16_t* src = P.q + (static_cast<int64_t>(b) * kH + h) * kD + p * 16;
+  const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(src + 8));
+  const float wv = p == 0 ? __ldg(P.w + static_cast<int64_t>(b) * kH + h) : 0.0f;
+  const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));  // the head's 8 threads
+  float sc, isc;
+  head_scale(m, flags, &sc, &isc);
+  uint32_t whi[4], wlo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h0, l0, h1, l1;
+    split_pair(x[4 * i] * sc, x[4 * i + 1] * sc, &h0, &l0);
+    split_pair(x[4 * i + 2] * sc, x[4 * i + 3] * sc, &h1, &l1);
+    whi[i] = h0 | (h1 << 16);
+    wlo[i] = l0 | (l1 << 16);
+  }
+  const uint32_t off = qbuf_offset(h, p);
+  *reinterpret_cast<uint4*>(S.qbuf[0][0] + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+  *reinterpret_cast<uint4*>(S.qbuf[0][1] + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+  if (p == 0) S.wbuf[0][h] = wv * isc;
+}
+
+// Prepares the queries of the CTA's later segments (the first one is prepared
+// in the prologue), each as soon as its slot is free.
 __device__ void role_qprep(const Params& P, Smem& S) {
   const int lane = threadIdx.x & 31;
   int32_t flags = 0;
-  int32_t b = S.plan.b0;
-  int64_t done = 0;
-  int64_t first = S.plan.lt0;
-  for (int seg = 0; done < S.plan.ntiles; ++seg) {
+  int64_t done = query_tiles(P, S.plan.b0) - S.plan.lt0;
+  int32_t b = next_nonempty(P, S.plan.b0 + 1);
+  for (int seg = 1; done < S.plan.ntiles; ++seg) {
     const int qs = seg & 1;
     int ok = 1;
     if (lane == 0)
@@ -585,9 +666,7 @@ __device__ void role_qprep(const Params& P, Smem& S) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.qfull[qs]));
-    const int64_t t = query_tiles(P, b) - first;
-    done += t;
-    first = 0;
+    done += query_tiles(P, b);
     b = next_nonempty(P, b + 1);
   }
 #pragma unroll
@@ -886,9 +965,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  {
+    int32_t qflags = 0;
+    prep_first_query(P, S, S.plan.b0, &qflags);
+    fence_proxy_async_smem();  // the MMA reads the query through the async proxy
+    if (qflags) atomicOr(&S.status, qflags);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) mbar_arrive(smem_u32(&S.qfull[0]));
 
   if (warp == kWarpIssuer) {
     role_issuer(P, S);
