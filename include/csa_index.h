@@ -62,7 +62,8 @@ extern "C" {
 typedef enum csa_status {
   CSA_OK = 0,
   CSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, k out of [1, CSA_MAX_K] ...   */
-  CSA_ERR_UNSUPPORTED = 2,   /* head_dim != 128 or num_heads != 64, too many SMs            */
+  CSA_ERR_UNSUPPORTED = 2,   /* head_dim != 128, num_heads other than 64 (or 128 where
+                                allowed), too many SMs                                       */
   CSA_ERR_ALIGNMENT = 3,     /* a pointer or stride breaks the alignment stated below       */
   CSA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than csa_index_workspace_bytes()  */
   CSA_ERR_CUDA = 5           /* a CUDA runtime call failed (launch, attribute, device query) */
@@ -143,7 +144,8 @@ size_t csa_index_workspace_bytes(const csa_index_args* args, int32_t k);
 
 /*
  * Scores of every visible record ("Retriever architecture": score = sigmoid of the
- * relu'd, head-weighted sum).
+ * relu'd, head-weighted sum). num_heads is 64 (the indexer) or 128 (the Level-1
+ * retriever's queries; this entry point and csa_index_logits only).
  *
  * scores  [num_q, score_stride] fp32 device memory, 4-byte aligned. Row b, column c:
  *           full mode      c = logical position n, for n < L
@@ -159,8 +161,8 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
 
 /*
  * csa_index_score writing the logits themselves (sum_h relu(k . q_h) * fused_w_h, before
- * the sigmoid), in the same layout, with the same arguments and errors. For callers that
- * combine several scorers before the sigmoid (two halves of a 128-head query).
+ * the sigmoid), in the same layout, with the same arguments and errors (64 or 128 heads).
+ * For callers that combine scorers before or after the sigmoid (the Level-1 recall).
  */
 csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t stride, void* stream);
 

@@ -60,9 +60,24 @@ constexpr int kSub = 2;                   // MMA sub-tiles per tile
 constexpr int kTile = kSub * kMmaRows;    // records per tile: the unit of every hand-off
 constexpr int kTilePages = kTile / kPage; // 4
 
-constexpr int kStages = 16;    // page stages in shared memory
 constexpr int kAStages = 2;    // TMEM A (key tile) stages: one per worker group
-constexpr int kDStages = 3;    // TMEM accumulator stages
+
+// Per head count H: page stages in shared memory and TMEM accumulator stages.
+// The indexer runs with 64 heads: an accumulator stage holds a whole tile
+// (2 sub-tiles x 64 columns). The scorer also runs with 128 heads (score and
+// logit modes, for the Level-1 recall): its query buffers double, which leaves
+// shared memory for 12 page stages, and a whole tile's accumulator would leave
+// TMEM room for one stage, which serialises the MMA and the epilogue; so its
+// stages hold one sub-tile (128 columns) each, taken and freed per sub-tile.
+template <int H> struct Geo;
+template <> struct Geo<64> {
+  static constexpr int kStages = 16, kDStages = 3, kDCols = 2 * 64;
+  static constexpr bool kSubStaged = false;
+};
+template <> struct Geo<128> {
+  static constexpr int kStages = 12, kDStages = 3, kDCols = 128;
+  static constexpr bool kSubStaged = true;
+};
 constexpr int kRing = 4;       // page-walker ring slots of 32 pages
 constexpr int kCap = 2048;     // candidate buffer of one segment (keys)
 constexpr int kKeyRing = 8;    // tiles of ranking keys between the workers and the selector
@@ -78,19 +93,23 @@ constexpr int kQEmptyCount = 1 + 4 * kWorkerGroups;  // MMA commit + every worke
 
 constexpr uint32_t kTmemCols = 512;
 // A stage: kSub x 32 columns (128 lanes x 128 e4m3 bytes per sub-tile);
-// D stage: kSub x 64 fp32 columns (128 records x 64 heads per sub-tile).
+// D stage: Geo<H>::kDCols fp32 columns (128 records x H heads per sub-tile it holds).
 __host__ __device__ constexpr uint32_t a_col(int s) { return static_cast<uint32_t>(s) * 32u * kSub; }
+template <int H>
 __host__ __device__ constexpr uint32_t d_col(int s) {
-  return 32u * kSub * kAStages + static_cast<uint32_t>(s) * 64u * kSub;
+  return 32u * kSub * kAStages + static_cast<uint32_t>(s) * Geo<H>::kDCols;
 }
-static_assert(d_col(kDStages) <= kTmemCols, "TMEM column map");
+static_assert(d_col<64>(Geo<64>::kDStages) <= kTmemCols && d_col<128>(Geo<128>::kDStages) <= kTmemCols,
+              "TMEM column map");
 static_assert(kAStages == kWorkerGroups, "each worker group owns one key stage");
-static_assert(kStages % 4 == 0 && kCap >= CSA_MAX_K + kTile, "stage and buffer sizes");
+static_assert(Geo<64>::kStages % 4 == 0 && Geo<128>::kStages % 4 == 0 && kCap >= CSA_MAX_K + kTile,
+              "stage and buffer sizes");
 
-// One MMA: 128 records x 64 heads x 32 bytes of K. A sub-tile takes 8 of them:
+// One MMA: 128 records x H heads x 32 bytes of K. A sub-tile takes 8 of them:
 // the query's hi term over K = 0..127, then its lo term over the same K, all
 // into one accumulator, so each head's column holds k . (q * 2^e_h) directly.
-constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 64);
+template <int H>
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, H);
 constexpr uint32_t kNaNBits = 0x7FC00000u;
 
 // Keys kept by a cut of a candidate buffer: at least k, at most half as many
@@ -320,20 +339,27 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
 
 // ------------------------------------------------------------------ shared memory
 
+template <int H>
 struct __align__(1024) Smem {
-  uint8_t qbuf[2][2][kH * kD];     // [slot][hi/lo] e4m3, K-major, 128-byte swizzle
+  static constexpr int kStages = Geo<H>::kStages, kDStages = Geo<H>::kDStages;
+  // Accumulator-ready signals, MMA -> worker group. The two groups take turns,
+  // so a group waits on every other signal; with fewer than three slots its
+  // next wait (same slot, same parity two phases later) could be satisfied by
+  // the completion it has just consumed.
+  static constexpr int kDSignals = kDStages >= 3 ? kDStages : 4;
+  uint8_t qbuf[2][2][H * kD];      // [slot][hi/lo] e4m3, K-major, 128-byte swizzle
   uint8_t pages[kStages][kPageBytes];
   uint64_t cand[kCap];
   uint64_t scratch[CSA_MAX_K];
   uint64_t keys[kKeyRing][kTile];  // a tile's admissible keys, worker -> selector: 64 per worker warp
   uint32_t kcnt[kKeyRing][4];      // keys in each worker warp's region of the slot
   uint64_t filt;                   // (segment << 32) | value word of the selector's current threshold
-  alignas(16) float wbuf[2][kH];   // read as float4
+  alignas(16) float wbuf[2][H];    // read as float4
   PageInfo ring[kRing * 32];
   PageInfo info[kStages];
   uint64_t full[kStages], empty[kStages];
   uint64_t afull[kAStages], aempty[kAStages];
-  uint64_t dfull[kDStages], dempty[kDStages];
+  uint64_t dfull[kDSignals], dempty[kDStages];
   uint64_t qfull[2], qempty[2];
   uint64_t rfull[kRing], rempty[kRing];
   uint64_t kfull[kKeyRing], kempty[kKeyRing];
@@ -347,25 +373,31 @@ struct __align__(1024) Smem {
   int32_t go[2];                   // selector leader's wait result, by tile parity
 };
 // alignment each field's accesses need: swizzle atoms, bulk-copy destinations, float4 loads
-static_assert(offsetof(Smem, qbuf) % 1024 == 0, "128-byte swizzle atoms need 1024-byte alignment");
-static_assert(offsetof(Smem, pages) % 16 == 0 && kPageBytes % 16 == 0, "bulk copies land on 16-byte boundaries");
-static_assert(offsetof(Smem, wbuf) % 16 == 0, "head weights are read as float4");
-static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, filt) % 8 == 0, "mbarriers and 64-bit words");
+template <int H>
+constexpr bool smem_layout_ok() {
+  return offsetof(Smem<H>, qbuf) % 1024 == 0 && offsetof(Smem<H>, pages) % 16 == 0 && kPageBytes % 16 == 0 &&
+         offsetof(Smem<H>, wbuf) % 16 == 0 && offsetof(Smem<H>, full) % 8 == 0 && offsetof(Smem<H>, filt) % 8 == 0;
+}
+static_assert(smem_layout_ok<64>() && smem_layout_ok<128>(),
+              "swizzle atoms 1024-byte, bulk copies and float4 loads 16-byte, mbarriers 8-byte aligned");
 
 // The worker-side filter of segment `seg`: a key whose value word is below the
 // returned word cannot reach the segment's best k (the selector has already
 // seen k keys at or above it); 0 admits every key. A word tagged with another
 // segment is stale and admits everything.
-__device__ __forceinline__ uint32_t filter_word(const Smem& S, int seg) {
+template <int H>
+__device__ __forceinline__ uint32_t filter_word(const Smem<H>& S, int seg) {
   const uint64_t f = *reinterpret_cast<const volatile uint64_t*>(&S.filt);
   return static_cast<uint32_t>(f >> 32) == static_cast<uint32_t>(seg) ? static_cast<uint32_t>(f) : 0u;
 }
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <int H>
+constexpr size_t kSmemBytes = sizeof(Smem<H>) + 1024;  // + alignment slack
+static_assert(kSmemBytes<64> <= 232448 && kSmemBytes<128> <= 232448, "shared memory budget");
 
-__device__ __forceinline__ Smem& smem_of(uint8_t* raw) {
-  return *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+template <int H>
+__device__ __forceinline__ Smem<H>& smem_of(uint8_t* raw) {
+  return *reinterpret_cast<Smem<H>*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
 // ------------------------------------------------------------------ roles
@@ -392,7 +424,11 @@ struct Cursor {
 __device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0; }
 
 
-__device__ void role_walker(const Params& P, Smem& S) {
+template <int H>
+__device__ void role_walker(const Params& P, Smem<H>& S) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
+  (void)kStages;
+  (void)kDStages;
   const int lane = threadIdx.x & 31;
   const int64_t npg = kTilePages * S.plan.ntiles;
   Cursor cur;
@@ -430,9 +466,14 @@ __device__ void role_walker(const Params& P, Smem& S) {
 // per-copy instruction latencies (ring read, barrier wait, expect_tx, copy) are
 // paid once per group instead of once per page.
 constexpr int kIssueLanes = 4;
-static_assert(kStages % kIssueLanes == 0 && 32 % kIssueLanes == 0, "issue groups");
+static_assert(Geo<64>::kStages % kIssueLanes == 0 && Geo<128>::kStages % kIssueLanes == 0 && 32 % kIssueLanes == 0,
+              "issue groups");
 
-__device__ void role_issuer(const Params& P, Smem& S) {
+template <int H>
+__device__ void role_issuer(const Params& P, Smem<H>& S) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
+  (void)kStages;
+  (void)kDStages;
   const int lane = threadIdx.x & 31;
   const int64_t npg = kTilePages * S.plan.ntiles;
   const uint64_t policy = policy_evict_first();
@@ -475,7 +516,11 @@ __device__ void role_issuer(const Params& P, Smem& S) {
     mbar_wait_drain(smem_u32(&S.full[p % kStages]), static_cast<uint32_t>((p / kStages) & 1));
 }
 
-__device__ void role_mma(const Params& P, Smem& S) {
+template <int H>
+__device__ void role_mma(const Params& P, Smem<H>& S) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
+  (void)kStages;
+  (void)kDStages;
   Cursor cur;
   cur.init(P, S.plan);
   const uint32_t tmem = S.tmem_base;
@@ -484,28 +529,53 @@ __device__ void role_mma(const Params& P, Smem& S) {
     const bool seg_start = (i == 0) || (cur.lt == 0);
     if (seg_start && i > 0) ++seg;
     const int qs = seg & 1;
-    const int ta = static_cast<int>(i % kAStages), td = static_cast<int>(i % kDStages);
+    const int ta = static_cast<int>(i % kAStages);
     if (seg_start &&
         !mbar_wait(smem_u32(&S.qfull[qs]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag))
       break;
     if (!mbar_wait(smem_u32(&S.afull[ta]), static_cast<uint32_t>((i / kAStages) & 1), &S.abort_flag)) break;
-    if (!mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((i / kDStages) & 1) ^ 1), &S.abort_flag))
-      break;
-    tc_fence_after();
+    if constexpr (Geo<H>::kSubStaged) {
+      bool ok = true;
 #pragma unroll
-    for (int sub = 0; sub < kSub; ++sub) {
-      const uint32_t dt = tmem + d_col(td) + 64 * sub;
-      const uint32_t at = tmem + a_col(ta) + 32 * sub;
+      for (int sub = 0; sub < kSub && ok; ++sub) {
+        // sub-tile u of the accumulator ring: its stage is free once the epilogue
+        // of the sub-tile kDStages earlier has read it
+        const int64_t u = kSub * i + sub;
+        const int td = static_cast<int>(u % kDStages);
+        ok = mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((u / kDStages) & 1) ^ 1), &S.abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + d_col<H>(td);
+        const uint32_t at = tmem + a_col(ta) + 32 * sub;
 #pragma unroll
-      for (int term = 0; term < 2; ++term) {
-        const uint32_t bq = smem_u32(S.qbuf[qs][term]);
+        for (int term = 0; term < 2; ++term) {
+          const uint32_t bq = smem_u32(S.qbuf[qs][term]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc, (term | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc<H>, (term | kk) != 0);
+        }
+      }
+      if (!ok) break;
+    } else {
+      const int td = static_cast<int>(i % kDStages);
+      if (!mbar_wait(smem_u32(&S.dempty[td]), static_cast<uint32_t>(((i / kDStages) & 1) ^ 1), &S.abort_flag))
+        break;
+      tc_fence_after();
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {
+        const uint32_t dt = tmem + d_col<H>(td) + H * sub;
+        const uint32_t at = tmem + a_col(ta) + 32 * sub;
+#pragma unroll
+        for (int term = 0; term < 2; ++term) {
+          const uint32_t bq = smem_u32(S.qbuf[qs][term]);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_e4m3_ts(dt, at + kk * 8, sdesc_kmajor_sw128(bq + kk * 32), kIdesc<H>, (term | kk) != 0);
+        }
       }
     }
     mma_commit(smem_u32(&S.aempty[ta]));
-    mma_commit(smem_u32(&S.dfull[td]));
+    mma_commit(smem_u32(&S.dfull[i % Smem<H>::kDSignals]));
     const bool seg_end = (i == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
     if (seg_end) mma_commit(smem_u32(&S.qempty[qs]));
     cur.advance(P);
@@ -557,24 +627,36 @@ __device__ __forceinline__ uint32_t qbuf_offset(int h, int chunk) {
 // loads are issued before the previous batch is processed: the first query of
 // a CTA is prepared while every CTA's first page copies load HBM, and a loop
 // that waits for memory once per head or per batch took about 11 us there.
-__device__ void prep_query(const Params& P, Smem& S, int32_t b, int qs, int32_t* flags) {
+template <int H>
+__device__ void prep_query(const Params& P, Smem<H>& S, int32_t b, int qs, int32_t* flags) {
   const int lane = threadIdx.x & 31;
-  const uint16_t* qrow = P.q + static_cast<int64_t>(b) * kH * kD;
-  const float* wrow = P.w + static_cast<int64_t>(b) * kH;
+  const uint16_t* qrow = P.q + static_cast<int64_t>(b) * H * kD;
+  const float* wrow = P.w + static_cast<int64_t>(b) * H;
   uint8_t* hi = S.qbuf[qs][0];
   uint8_t* lo = S.qbuf[qs][1];
-  const float w_first = __ldg(wrow + lane), w_second = __ldg(wrow + 32 + lane);  // heads lane, lane + 32
-  {
-    const char* base = reinterpret_cast<const char*>(qrow);
+  // 64 heads: each lane holds the weights of heads lane and lane + 32. 128 heads: the raw
+  // weights go to the slot first and each is scaled in place once its head's scale is known
+  // (four per lane would be indexed by a run-time head).
+  float w_first = 0.0f, w_second = 0.0f;
+  if constexpr (H == 64) {
+    w_first = __ldg(wrow + lane);
+    w_second = __ldg(wrow + 32 + lane);
+  } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (lane + 32 * j) * 128));
+    for (int j = 0; j < H / 32; ++j) S.wbuf[qs][32 * j + lane] = __ldg(wrow + 32 * j + lane);
+    __syncwarp();
+  }
+  {
+    const char* base = reinterpret_cast<const char*>(qrow);  // H rows of 256 bytes: H / 16 lines per lane
+#pragma unroll
+    for (int j = 0; j < H / 16; ++j) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (lane + 32 * j) * 128));
   }
   uint2 raw[8], nxt[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) raw[j] = __ldg(reinterpret_cast<const uint2*>(qrow + j * kD + lane * 4));
 #pragma unroll 1
-  for (int h0 = 0; h0 < kH; h0 += 8) {
-    if (h0 + 8 < kH) {
+  for (int h0 = 0; h0 < H; h0 += 8) {
+    if (h0 + 8 < H) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) nxt[j] = __ldg(reinterpret_cast<const uint2*>(qrow + (h0 + 8 + j) * kD + lane * 4));
     }
@@ -602,7 +684,11 @@ __device__ void prep_query(const Params& P, Smem& S, int32_t b, int qs, int32_t*
       const uint32_t off = qbuf_offset(h, lane >> 2) + (lane & 3) * 4;
       *reinterpret_cast<uint32_t*>(hi + off) = whi;
       *reinterpret_cast<uint32_t*>(lo + off) = wlo;
-      if (lane == (h & 31)) S.wbuf[qs][h] = (h < 32 ? w_first : w_second) * isc;
+      if constexpr (H == 64) {
+        if (lane == (h & 31)) S.wbuf[qs][h] = (h < 32 ? w_first : w_second) * isc;
+      } else {
+        if (lane == (h & 31)) S.wbuf[qs][h] *= isc;
+      }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) raw[j] = nxt[j];
@@ -613,13 +699,17 @@ __device__ void prep_query(const Params& P, Smem& S, int32_t b, int qs, int32_t*
 // before any page copy is in flight, into query slot 0: thread t takes the 16
 // elements 16p .. 16p+15 of head h = t / 8 (p = t % 8), so that the row's loads
 // are all issued at once. Same arithmetic and layout as prep_query.
-static_assert(kThreads == kH * (kD / 16), "one thread per 16 elements of a query row");
-__device__ void prep_first_query(const Params& P, Smem& S, int32_t b, int32_t* flags) {
-  const int tid = threadIdx.x, h = tid >> 3, p = tid & 7;
-  const uint16_t* src = P.q + (static_cast<int64_t>(b) * kH + h) * kD + p * 16;
+static_assert(kThreads == 64 * (kD / 16), "64 heads per pass, one thread per 16 elements");
+template <int H>
+__device__ void prep_first_query(const Params& P, Smem<H>& S, int32_t b, int32_t* flags) {
+  const int tid = threadIdx.x, p = tid & 7;
+#pragma unroll
+  for (int pass = 0; pass < H / 64; ++pass) {
+  const int h = (tid >> 3) + 64 * pass;
+  const uint16_t* src = P.q + (static_cast<int64_t>(b) * H + h) * kD + p * 16;
   const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(src));
   const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(src + 8));
-  const float wv = p == 0 ? __ldg(P.w + static_cast<int64_t>(b) * kH + h) : 0.0f;
+  const float wv = p == 0 ? __ldg(P.w + static_cast<int64_t>(b) * H + h) : 0.0f;
   const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
   float x[16];
 #pragma unroll
@@ -647,11 +737,16 @@ __device__ void prep_first_query(const Params& P, Smem& S, int32_t b, int32_t* f
   *reinterpret_cast<uint4*>(S.qbuf[0][0] + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
   *reinterpret_cast<uint4*>(S.qbuf[0][1] + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
   if (p == 0) S.wbuf[0][h] = wv * isc;
+  }
 }
 
 // Prepares the queries of the CTA's later segments (the first one is prepared
 // in the prologue), each as soon as its slot is free.
-__device__ void role_qprep(const Params& P, Smem& S) {
+template <int H>
+__device__ void role_qprep(const Params& P, Smem<H>& S) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
+  (void)kStages;
+  (void)kDStages;
   const int lane = threadIdx.x & 31;
   int32_t flags = 0;
   int64_t done = query_tiles(P, S.plan.b0) - S.plan.lt0;
@@ -681,8 +776,9 @@ __device__ void role_qprep(const Params& P, Smem& S) {
 // Once the MMA of own tile t is done, the group's key stage is free: the warp
 // loads own tile t + kWorkerGroups first, so that its MMA overlaps the
 // epilogue of t. The warps never wait on each other.
-template <bool kTopk>
-__device__ void role_worker(const Params& P, Smem& S) {
+template <bool kTopk, int H>
+__device__ void role_worker(const Params& P, Smem<H>& S) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
   const int wi = (threadIdx.x >> 5) - kWarpWorker;
   const int group = wi >> 2;
   const int q = wi & 3;
@@ -747,10 +843,10 @@ __device__ void role_worker(const Params& P, Smem& S) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) a0[j] = a1[j] = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < kH; c += 16) {  // heads c .. c+15 of both records
+    for (int c = 0; c < H; c += 16) {  // heads c .. c+15 of both records
       uint32_t x0[16], x1[16];
-      tmem_ld16(tmem + d_col(td) + c + lane_off, x0);
-      tmem_ld16(tmem + d_col(td) + 64 + c + lane_off, x1);
+      tmem_ld16(tmem + d_col<H>(td) + c + lane_off, x0);
+      tmem_ld16(tmem + d_col<H>(td) + H + c + lane_off, x1);
       tmem_wait_ld();
       float4 w4[4];
 #pragma unroll
@@ -774,17 +870,67 @@ __device__ void role_worker(const Params& P, Smem& S) {
     logit[1] = fabsf(s1) * (((a1[0] + a1[4]) + (a1[1] + a1[5])) + ((a1[2] + a1[6]) + (a1[3] + a1[7])));
   };
 
+  // Logit of this lane's record in the sub-tile whose accumulator is stage td
+  // (sub-staged accumulators): two 16-head chunks per TMEM wait, two sums.
+  auto logit_one = [&](int td, uint32_t scb, int seg) -> float {
+    const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
+    const float s = __uint_as_float(scb);
+    const float g = s < 0.0f ? -1.0f : 1.0f;
+    const bool all_pos = __all_sync(0xFFFFFFFFu, g > 0.0f);
+    float a0[8], a1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a0[j] = a1[j] = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < H; c += 32) {  // heads c .. c+31
+      uint32_t x0[16], x1[16];
+      tmem_ld16(tmem + d_col<H>(td) + c + lane_off, x0);
+      tmem_ld16(tmem + d_col<H>(td) + c + 16 + lane_off, x1);
+      tmem_wait_ld();
+      float4 w4[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w4[j] = wv[(c >> 2) + j];
+      const float* w = reinterpret_cast<const float*>(w4);
+      if (all_pos) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          a0[j & 7] = fmaf(fmaxf(__uint_as_float(x0[j]), 0.f), w[j], a0[j & 7]);
+          a1[j & 7] = fmaf(fmaxf(__uint_as_float(x1[j]), 0.f), w[16 + j], a1[j & 7]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          a0[j & 7] = fmaf(fmaxf(g * __uint_as_float(x0[j]), 0.f), w[j], a0[j & 7]);
+          a1[j & 7] = fmaf(fmaxf(g * __uint_as_float(x1[j]), 0.f), w[16 + j], a1[j & 7]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a0[j] += a1[j];
+    return fabsf(s) * (((a0[0] + a0[4]) + (a0[1] + a0[5])) + ((a0[2] + a0[6]) + (a0[3] + a0[7])));
+  };
+
   // Epilogue of own tile i of row b, local tile lt, segment `seg`; the caller
   // has seen the tile's accumulator complete.
   auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, const uint32_t (&sc)[kSub],
                       const uint32_t (&pos)[kSub]) -> bool {
-    const int td = static_cast<int>(i % kDStages);
     tc_fence_after();
     float logit[kSub];
-    logits_of(td, sc, seg, logit);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
+    if constexpr (Geo<H>::kSubStaged) {
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {  // each stage is freed as soon as it is read
+        const int td = static_cast<int>((kSub * i + sub) % kDStages);
+        logit[sub] = logit_one(td, sc[sub], seg);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
+      }
+    } else {
+      const int td = static_cast<int>(i % kDStages);
+      logits_of(td, sc, seg, logit);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
+    }
 
     if constexpr (!kTopk) {
       float* out = P.scores + static_cast<int64_t>(b) * P.score_stride + lt * kTile + row;
@@ -839,7 +985,8 @@ __device__ void role_worker(const Params& P, Smem& S) {
         wseg = seg;
       }
       // MMA of tile t done: its accumulator is ready and the group's key stage is free
-      const bool okd = mbar_wait(smem_u32(&S.dfull[t % kDStages]), static_cast<uint32_t>((t / kDStages) & 1),
+      constexpr int kDSignals = Smem<H>::kDSignals;
+      const bool okd = mbar_wait(smem_u32(&S.dfull[t % kDSignals]), static_cast<uint32_t>((t / kDSignals) & 1),
                                  &S.abort_flag);
       if (!__all_sync(0xFFFFFFFFu, okd)) break;
       if (t + kWorkerGroups < nt) {
@@ -867,7 +1014,11 @@ __device__ void role_worker(const Params& P, Smem& S) {
 // buffer, cuts the buffer back to between k and loose_keep(k) keys when it
 // fills, publishes the new threshold to the workers, and writes each segment's
 // survivors (at most loose_keep(k), unsorted) to workspace slot (row + CTA).
-__device__ void role_select(const Params& P, Smem& S) {
+template <int H>
+__device__ void role_select(const Params& P, Smem<H>& S) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
+  (void)kStages;
+  (void)kDStages;
   const int g = threadIdx.x - kWarpSelect * 32;
   const int sw = g >> 5, lane = g & 31;
   Cursor cur;
@@ -913,10 +1064,11 @@ __device__ void role_select(const Params& P, Smem& S) {
   }
 }
 
-template <bool kTopk>
+template <bool kTopk, int H>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
+  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
   extern __shared__ uint8_t smem_raw[];
-  Smem& S = smem_of(smem_raw);
+  Smem<H>& S = smem_of<H>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
     S.plan.flags = 0;
@@ -941,10 +1093,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
       mbar_init(smem_u32(&S.afull[s]), 4);  // the four warps of the loading worker group
       mbar_init(smem_u32(&S.aempty[s]), 1);
     }
-    for (int s = 0; s < kDStages; ++s) {
-      mbar_init(smem_u32(&S.dfull[s]), 1);
-      mbar_init(smem_u32(&S.dempty[s]), 4);
-    }
+    for (int s = 0; s < Smem<H>::kDSignals; ++s) mbar_init(smem_u32(&S.dfull[s]), 1);
+    for (int s = 0; s < kDStages; ++s) mbar_init(smem_u32(&S.dempty[s]), 4);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&S.qfull[s]), 1);
       mbar_init(smem_u32(&S.qempty[s]), kQEmptyCount);
@@ -985,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
   } else if (warp == kWarpQprep) {
     role_qprep(P, S);
   } else if (warp < kWarpSelect) {
-    role_worker<kTopk>(P, S);
+    role_worker<kTopk, H>(P, S);
   } else if (kTopk) {
     role_select(P, S);
   }
@@ -1233,7 +1383,7 @@ size_t slots_offset_for(int32_t num_q) { return (4 * (static_cast<size_t>(num_q)
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-enum { kNeedQ = 1, kNeedKv = 2 };
+enum { kNeedQ = 1, kNeedKv = 2, kAllowWide = 4 };  // kAllowWide: 128 heads accepted as well as 64
 
 csa_status check_args(const csa_index_args* a, int need) {
   if (!a) return CSA_ERR_INVALID_ARG;
@@ -1249,7 +1399,8 @@ csa_status check_args(const csa_index_args* a, int need) {
   }
   if (a->dev_status && !aligned(a->dev_status, 4)) return CSA_ERR_ALIGNMENT;
   if (need & kNeedQ) {
-    if (a->num_heads != kH || a->head_dim != kD) return CSA_ERR_UNSUPPORTED;
+    if (a->head_dim != kD || !(a->num_heads == kH || ((need & kAllowWide) && a->num_heads == 2 * kH)))
+      return CSA_ERR_UNSUPPORTED;
     if (!a->q || !a->fused_w) return CSA_ERR_INVALID_ARG;
     if (!aligned(a->q, 16) || !aligned(a->fused_w, 4)) return CSA_ERR_ALIGNMENT;
   }
@@ -1275,10 +1426,12 @@ csa_status device_setup(int* sms) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return CSA_ERR_CUDA;
     if (n * kTopkCtasPerSm > CSA_MAX_CTAS) return CSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+    if (cudaFuncSetAttribute(score_kernel<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes<64>)) != cudaSuccess ||
+        cudaFuncSetAttribute(score_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes<64>)) != cudaSuccess ||
+        cudaFuncSetAttribute(score_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes<128>)) != cudaSuccess ||
         cudaFuncSetAttribute(merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(MergeSmem) + 16)) != cudaSuccess ||
         cudaFuncSetAttribute(merge_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1322,6 +1475,15 @@ csa_status launch_status() { return cudaGetLastError() == cudaSuccess ? CSA_OK :
 
 }  // namespace
 
+// Score or logit mode (P.raw_logits) of the scoring kernel for 64 or 128 heads.
+void launch_score(const Params& P, int32_t num_heads, int sms, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_heads == 2 * kH)
+    score_kernel<false, 128><<<sms, kThreads, kSmemBytes<128>, s>>>(P);
+  else
+    score_kernel<false, 64><<<sms, kThreads, kSmemBytes<64>, s>>>(P);
+}
+
 extern "C" {
 
 int32_t csa_index_abi_version(void) { return CSA_ABI_VERSION; }
@@ -1345,7 +1507,7 @@ size_t csa_index_workspace_bytes(const csa_index_args* args, int32_t k) {
 }
 
 csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t score_stride, void* stream) {
-  csa_status st = check_args(args, kNeedQ | kNeedKv);
+  csa_status st = check_args(args, kNeedQ | kNeedKv | kAllowWide);
   if (st != CSA_OK) return st;
   if (args->num_q == 0) return CSA_OK;
   if (!scores) return CSA_ERR_INVALID_ARG;
@@ -1357,12 +1519,12 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
   P.scores = scores;
   P.score_stride = score_stride;
   P.grid = sms;
-  score_kernel<false><<<sms, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(P);
+  launch_score(P, args->num_heads, sms, stream);
   return launch_status();
 }
 
 csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t stride, void* stream) {
-  csa_status st = check_args(args, kNeedQ | kNeedKv);
+  csa_status st = check_args(args, kNeedQ | kNeedKv | kAllowWide);
   if (st != CSA_OK) return st;
   if (args->num_q == 0) return CSA_OK;
   if (!logits) return CSA_ERR_INVALID_ARG;
@@ -1375,7 +1537,7 @@ csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t s
   P.score_stride = stride;
   P.grid = sms;
   P.raw_logits = 1;
-  score_kernel<false><<<sms, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(P);
+  launch_score(P, args->num_heads, sms, stream);
   return launch_status();
 }
 
@@ -1403,7 +1565,7 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
   P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
   P.grid = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  score_kernel<true><<<sms, kThreads, kSmemBytes, s>>>(P);
+  score_kernel<true, 64><<<sms, kThreads, kSmemBytes<64>, s>>>(P);
   if ((st = launch_status()) != CSA_OK) return st;
   if (event && cudaEventRecord(static_cast<cudaEvent_t>(event), s) != cudaSuccess) return CSA_ERR_CUDA;
   merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
@@ -1495,7 +1657,7 @@ extern "C" csa_status csa_index_score_topk_fused_static(const csa_index_args* ar
   P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
   P.grid = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  score_kernel<true><<<sms, kThreads, kSmemBytes, s>>>(P);
+  score_kernel<true, 64><<<sms, kThreads, kSmemBytes<64>, s>>>(P);
   if ((st = launch_status()) != CSA_OK) return st;
   merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
   return launch_status();

@@ -7,10 +7,9 @@
 // chunk and, per query row, the ascending list of logical pages that hold a
 // resident chunk (the Level-2 resident list).
 //
-// Each layer's 128-head logit is the sum of two 64-head logits (relu is taken
-// per head, before the head-weighted sum), so the scoring kernel runs once per
-// half of each layer's query (csa_index_logits) and a small kernel adds the
-// halves, applies the sigmoid and folds the layer into the combined score.
+// The scoring kernel runs once per layer with the layer's 128-head query in its
+// logit mode (csa_index_logits), reading each layer's cache once; a small kernel
+// applies the sigmoid and folds the layer into the combined score.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -20,28 +19,21 @@
 
 namespace {
 
-constexpr int kHalfHeads = 64, kD = 128, kPage = 64;
+constexpr int kHeads = 128, kD = 128, kPage = 64;
 constexpr int kMaxLayers = 8;
 constexpr int kFinalThreads = 256;  // one page of the window per thread
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: one 64-head half of a layer's query and weights, the two halves'
-// logits, and the running combined score.
+// Workspace: one layer's logits and the running combined score.
 struct Layout {
-  size_t q, w, la, lb, acc, total;
+  size_t la, acc, total;
 };
 
 Layout layout_of(int64_t num_q, int64_t stride) {
   Layout L;
   size_t off = 0;
-  L.q = off;
-  off += round256(static_cast<size_t>(num_q) * kHalfHeads * kD * 2);
-  L.w = off;
-  off += round256(static_cast<size_t>(num_q) * kHalfHeads * 4);
   L.la = off;
-  off += round256(static_cast<size_t>(num_q) * stride * 4);
-  L.lb = off;
   off += round256(static_cast<size_t>(num_q) * stride * 4);
   L.acc = off;
   off += round256(static_cast<size_t>(num_q) * stride * 4);
@@ -69,11 +61,11 @@ __device__ __forceinline__ int64_t row_len(const Rows& R, int32_t b) {
   return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
-// acc = layer 0 ? s : combine(acc, s), s = sigmoid(la + lb), for the visible
+// acc = layer 0 ? s : combine(acc, s), s = sigmoid(la), for the visible
 // positions of row blockIdx.x (blockIdx.y strides over the positions). A
 // position on a page this layer's page table maps out of range was not scored
 // (the scorer flags it); it counts 0 in this layer.
-__global__ void combine_kernel(const float* la, const float* lb, float* acc, int64_t stride, Rows R,
+__global__ void combine_kernel(const float* la, float* acc, int64_t stride, Rows R,
                                const int32_t* page_table, int64_t num_pages, int layer, int ensemble) {
   const int32_t b = blockIdx.x;
   const int64_t L = row_len(R, b);
@@ -83,7 +75,7 @@ __global__ void combine_kernel(const float* la, const float* lb, float* acc, int
        n += static_cast<int64_t>(gridDim.y) * blockDim.x) {
     const int64_t o = static_cast<int64_t>(b) * stride + n;
     const int32_t phys = pt[n / kPage];
-    const float s = phys < 0 || phys >= num_pages ? 0.0f : 1.0f / (1.0f + expf(-(la[o] + lb[o])));
+    const float s = phys < 0 || phys >= num_pages ? 0.0f : 1.0f / (1.0f + expf(-la[o]));
     acc[o] = layer == 0 ? s : (ensemble == CSA_ENSEMBLE_MAX ? fmaxf(acc[o], s) : acc[o] + s);
   }
 }
@@ -153,7 +145,7 @@ extern "C" csa_status csa_recall_level1(const csa_recall_args* a, void* ws, size
   const csa_index_args& L0 = a->layers[0];
   for (int l = 0; l < a->n_layers; ++l) {
     const csa_index_args& L = a->layers[l];
-    if (!same_rows(L0, L) || L.num_heads != 2 * kHalfHeads || L.head_dim != kD || L.resident || L.n_resident)
+    if (!same_rows(L0, L) || L.num_heads != kHeads || L.head_dim != kD || L.resident || L.n_resident)
       return CSA_ERR_INVALID_ARG;
   }
   const int64_t num_q = L0.num_q;
@@ -170,7 +162,6 @@ extern "C" csa_status csa_recall_level1(const csa_recall_args* a, void* ws, size
   if (reinterpret_cast<uintptr_t>(ws) & 255) return CSA_ERR_ALIGNMENT;
   uint8_t* base = static_cast<uint8_t*>(ws);
   float* la = reinterpret_cast<float*>(base + W.la);
-  float* lb = reinterpret_cast<float*>(base + W.lb);
   float* acc = reinterpret_cast<float*>(base + W.acc);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Rows R{L0.q_len, L0.q_req, L0.num_req, L0.pt_stride};
@@ -180,29 +171,16 @@ extern "C" csa_status csa_recall_level1(const csa_recall_args* a, void* ws, size
     return CSA_ERR_CUDA;
   for (int l = 0; l < a->n_layers; ++l) {
     const csa_index_args& L = a->layers[l];
-    if (!L.q || !L.fused_w) return CSA_ERR_INVALID_ARG;
-    for (int h = 0; h < 2; ++h) {
-      // this half of the layer's query and weights, rows packed
-      const size_t qrow = static_cast<size_t>(kHalfHeads) * kD * 2, wrow = static_cast<size_t>(kHalfHeads) * 4;
-      if (cudaMemcpy2DAsync(base + W.q, qrow, static_cast<const uint8_t*>(L.q) + h * qrow, 2 * qrow, qrow,
-                            static_cast<size_t>(num_q), cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-          cudaMemcpy2DAsync(base + W.w, wrow, reinterpret_cast<const uint8_t*>(L.fused_w) + h * wrow, 2 * wrow,
-                            wrow, static_cast<size_t>(num_q), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-        return CSA_ERR_CUDA;
-      csa_index_args half = L;
-      half.q = base + W.q;
-      half.fused_w = reinterpret_cast<const float*>(base + W.w);
-      half.num_heads = kHalfHeads;
-      half.q_len = L0.q_len;
-      half.q_req = L0.q_req;
-      half.dev_status = L0.dev_status;
-      const csa_status st = csa_index_logits(&half, h == 0 ? la : lb, a->keep_stride, stream);
-      if (st != CSA_OK) return st;
-    }
+    csa_index_args layer = L;
+    layer.q_len = L0.q_len;  // every layer scores layer 0's rows
+    layer.q_req = L0.q_req;
+    layer.dev_status = L0.dev_status;
+    const csa_status st = csa_index_logits(&layer, la, a->keep_stride, stream);
+    if (st != CSA_OK) return st;
     int64_t gy = (static_cast<int64_t>(sms) * 8 + num_q - 1) / num_q;  // about 8 CTAs per SM in all
     gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
     combine_kernel<<<dim3(static_cast<unsigned>(num_q), static_cast<unsigned>(gy)), 256, 0, s>>>(
-        la, lb, acc, a->keep_stride, R, L.page_table, L.num_pages, l, a->ensemble);
+        la, acc, a->keep_stride, R, L.page_table, L.num_pages, l, a->ensemble);
     if (cudaGetLastError() != cudaSuccess) return CSA_ERR_CUDA;
   }
   select_kernel<<<static_cast<unsigned>(num_q), kFinalThreads, 0, s>>>(

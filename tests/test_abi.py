@@ -85,7 +85,7 @@ def _fake_args(**kw):
 
 
 @pytest.mark.parametrize("change,want", [
-    (dict(head_dim=64), 2), (dict(num_heads=128), 2), (dict(q=0), 1), (dict(q=0x10008), 3),
+    (dict(head_dim=64), 2), (dict(num_heads=96), 2), (dict(num_heads=256), 2), (dict(q=0), 1), (dict(q=0x10008), 3),
     (dict(kv=0x30004), 3), (dict(page_stride_bytes=8440), 1), (dict(page_stride_bytes=8456), 3),
     (dict(num_q=-1), 1), (dict(reserved0=1), 1), (dict(q_len=0), 1), (dict(num_req=2), 1),
     (dict(resident=0x60000), 1), (dict(num_pages=0), 1), (dict(page_table=0x40002), 3),
@@ -121,6 +121,17 @@ def test_static_scratch_variant_validates_on_the_host(lib):
     assert f(ctypes.addressof(a), 0, 0x1000, 0x2000, None) == 1
     assert f(ctypes.addressof(a), 512, 0x1002, 0x2000, None) == 3
     assert f(ctypes.addressof(_fake_args(head_dim=64)), 512, 0x1000, 0x2000, None) == 2
+
+
+def test_128_heads_only_in_score_and_logit_modes(lib):
+    """The scorer takes 64 or 128 heads; the top-k entry points only 64."""
+    a = _fake_args(num_heads=128, num_q=0)
+    assert lib.csa_index_score(ctypes.byref(a), None, 0, None) == 0
+    assert lib.csa_index_logits(ctypes.byref(a), None, 0, None) == 0
+    a = _fake_args(num_heads=128)
+    ws = native.workspace_bytes(a, 512)
+    assert lib.csa_index_score_topk_fused(ctypes.byref(a), 512, 0x1000, 0x2000, 0x3000, ws, None) == 2
+    assert lib.csa_index_logits(ctypes.byref(a), 0x70002, 256, None) == 3  # validated like 64 heads
 
 
 def test_empty_batch_is_a_no_op(lib):

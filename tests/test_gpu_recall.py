@@ -118,14 +118,12 @@ def mid_threshold(osc, L):
 
 @pytest.mark.parametrize("heads", [64, 128])
 def test_logits_match_the_oracle(heads):
+    """Both head counts of the scorer, against the oracle's logits; 128 heads also
+    through csa_index_score."""
     w = synth.make_workload("lg", num_q=4, history=[3000, 700, 64, 1], seed=61)
     if heads == 128:
         w = synth.level1_layers(w, 1, seed=62)[0]
     prob = native.Problem.from_workload(w)
-    if heads == 128:  # the scorer takes 64 heads; 128 is the recall's business
-        with pytest.raises(native.CsaError):
-            native.csa_index_logits(prob)
-        return
     lg = native.csa_index_logits(prob)
     torch.cuda.synchronize()
     lg = lg.cpu().numpy().astype(np.float64)
@@ -136,6 +134,34 @@ def test_logits_match_the_oracle(heads):
     # and the sigmoid of them is what csa_index_score writes
     s = native.csa_index_score(prob).cpu().numpy().astype(np.float64)
     assert np.max(np.abs(_parity.sigmoid(lg[valid]) - s[valid])) <= 1e-6
+
+
+def test_128_head_logits_large_dynamic_range_and_bad_pages():
+    """128-head queries whose heads span 2^-20..2^20, weights scaled by 2^-6..2^6,
+    one page out of range (flagged, its records not written)."""
+    w = synth.level1_layers(synth.make_workload("dr", num_q=3, history=[2500, 900, 130], seed=64), 1, seed=65)[0]
+    rng = np.random.default_rng(66)
+    qf = rng.standard_normal((3, 128, 128)).astype(np.float32)
+    qf *= np.float32(2.0) ** rng.integers(-20, 21, size=(3, 128, 1)).astype(np.float32)
+    w.q = _pins.bf16_bits(qf).reshape(3, 128, 128)
+    w.fused_w = w.fused_w * (np.float32(2.0) ** rng.integers(-6, 7, size=(3, 128)).astype(np.float32))
+    w.page_table = w.page_table.copy()
+    w.page_table[1, 3] = w.num_pages + 5
+    prob = native.Problem.from_workload(w)
+    lg = native.csa_index_logits(prob)
+    torch.cuda.synchronize()
+    assert int(prob.dev_status.item()) == native.DEV_PAGE_OOB
+    lg = lg.cpu().numpy().astype(np.float64)
+    olg, valid, flags = oracle.logits(oracle.Problem(w), lg.shape[1])
+    assert flags == oracle.PAGE_OOB
+    assert np.all(np.isnan(lg[~valid])) and not np.any(np.isnan(lg[valid]))
+    # weights of both signs make terms near 1e6 cancel: fp32 error scales with
+    # sum_h relu(k . q_h) |w_h|, which is the oracle's logit with |w|
+    mag = synth.Workload(name="mag", q=w.q, fused_w=np.abs(w.fused_w), kv=w.kv, page_table=w.page_table,
+                         q_len=w.q_len)
+    scale, _, _ = oracle.logits(oracle.Problem(mag), lg.shape[1])
+    d = np.abs(lg[valid] - olg[valid])
+    assert np.all(d <= _parity.STRICT_LOGIT_TOL * (1.0 + scale[valid])), (d / (1.0 + scale[valid])).max()
 
 
 # ------------------------------------------------------------------ recall against the oracle
