@@ -244,3 +244,22 @@ def test_recall_deterministic():
     b = run_gpu(layers, True, 0.5, 2, 100, problems=P)
     for x, y in zip(a, b):
         assert np.array_equal(x, y, equal_nan=True)
+
+
+def test_128_head_scores_resident_mode():
+    """The 128-head scorer over a resident page list (csa_index_score), against the
+    oracle's scores in the resident column layout."""
+    w = synth.make_workload("r128", num_q=3, history=[64 * 40 + 17, 64 * 9, 64 * 30], resident_pages=7, seed=71)
+    w = dataclasses.replace(synth.level1_layers(w, 1, seed=72)[0], resident=w.resident, n_resident=w.n_resident)
+    prob = native.Problem.from_workload(w)
+    sc = native.csa_index_score(prob)
+    torch.cuda.synchronize()
+    assert int(prob.dev_status.item()) == 0
+    _parity.check_scores(w, sc.cpu().numpy())
+
+
+def test_recall_eight_layers_mean():
+    """The largest layer count, mean ensemble, threshold between two oracle scores."""
+    layers = _pins.recall_layers(8, 2, [1500, 700], seed=73)
+    _, osc, _, _ = oracle.recall([oracle.Problem(w) for w in layers], True, 2.0, 0, 0)
+    check(layers, True, mid_threshold(osc[0], 1500), sink=1, recent=33)
