@@ -594,8 +594,9 @@ def run_recall(args):
     alg = args.layers * records * 132 + records * 5
     peak, src = measured_peaks()
     gbs = alg / (ms * 1e-3) / 1e9
-    # kernels per step: per layer two scorer launches and one combine, then one select
-    launches = steps * (3 * args.layers + 1)
+    # kernels per step: one scorer launch per layer, then the keep and list kernels
+    # (the zeroing of the combined-score plane is a memset)
+    launches = steps * (args.layers + 2)
     line = {
         "metric": "Level-1 recall chunks/s and HBM GB/s (fraction of peak)",
         "value": records / (ms * 1e-3),

@@ -45,6 +45,7 @@
 #include <mutex>
 
 #include "csa_index.h"
+#include "csa_internal.h"
 #include "csa_ptx.cuh"
 #include "csa_select.cuh"
 
@@ -154,6 +155,7 @@ struct Params {
   int32_t k;
   int32_t grid;         // CTAs of the phase-1 kernel (slot numbering)
   int32_t raw_logits;   // score mode: write the logit instead of its sigmoid
+  int32_t fold;         // score mode: 0 store, CSA_FOLD_MAX / CSA_FOLD_ADD fold the score into the output
 };
 
 struct PageInfo {
@@ -936,8 +938,11 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
       float* out = P.scores + static_cast<int64_t>(b) * P.score_stride + lt * kTile + row;
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
-        if (!isnan(__uint_as_float(sc[sub])))
-          out[kMmaRows * sub] = P.raw_logits ? logit[sub] : __frcp_rn(1.0f + __expf(-logit[sub]));
+        if (!isnan(__uint_as_float(sc[sub]))) {
+          const float v = P.raw_logits ? logit[sub] : __frcp_rn(1.0f + __expf(-logit[sub]));
+          float* o = out + kMmaRows * sub;
+          *o = P.fold == 0 ? v : (P.fold == CSA_FOLD_MAX ? fmaxf(*o, v) : *o + v);
+        }
     } else {
       const int slot = static_cast<int>(i % kKeyRing);
       const bool ok2 = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((i / kKeyRing) & 1) ^ 1),
@@ -1540,6 +1545,28 @@ csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t s
   launch_score(P, args->num_heads, sms, stream);
   return launch_status();
 }
+
+}  // extern "C"
+
+csa_status csa_score_fold(const csa_index_args* args, float* acc, int64_t stride, int fold, void* stream) {
+  csa_status st = check_args(args, kNeedQ | kNeedKv | kAllowWide);
+  if (st != CSA_OK) return st;
+  if (args->num_q == 0) return CSA_OK;
+  if (!acc || args->resident || (fold != CSA_FOLD_MAX && fold != CSA_FOLD_ADD)) return CSA_ERR_INVALID_ARG;
+  if (!aligned(acc, 4)) return CSA_ERR_ALIGNMENT;
+  if (stride < min_score_stride(args)) return CSA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != CSA_OK) return st;
+  Params P = params_of(args);
+  P.scores = acc;
+  P.score_stride = stride;
+  P.grid = sms;
+  P.fold = fold;
+  launch_score(P, args->num_heads, sms, stream);
+  return launch_status();
+}
+
+extern "C" {
 
 csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int32_t* idx, float* vals, void* ws,
                                       size_t ws_bytes, void* stream) {

@@ -7,36 +7,44 @@
 // chunk and, per query row, the ascending list of logical pages that hold a
 // resident chunk (the Level-2 resident list).
 //
-// The scoring kernel runs once per layer with the layer's 128-head query in its
-// logit mode (csa_index_logits), reading each layer's cache once; a small kernel
-// applies the sigmoid and folds the layer into the combined score.
+// The combined score lives in a workspace plane, zeroed first; the scoring
+// kernel runs once per layer with the layer's 128-head query and folds each
+// visible record's score into the plane (max, or sum for the mean) in its
+// epilogue, so each layer's cache is read once and no per-layer plane is
+// written. A record the layer cannot read (a page out of range) leaves the
+// plane as it is: it counts 0 for that layer. A kernel over (row, window of
+// pages) then writes keep, the scores and a flag per page, and a small kernel
+// per row compacts the flags into the page list.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
 
 #include "csa_index.h"
+#include "csa_internal.h"
 
 namespace {
 
 constexpr int kHeads = 128, kD = 128, kPage = 64;
 constexpr int kMaxLayers = 8;
-constexpr int kFinalThreads = 256;  // one page of the window per thread
+constexpr int kWinPages = 64;          // pages per CTA of the keep kernel
+constexpr int kWinThreads = 256;
+constexpr int kListThreads = 256;      // pages per pass of the list kernel
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: one layer's logits and the running combined score.
+// Workspace: the combined score plane and one flag per (row, logical page).
 struct Layout {
-  size_t la, acc, total;
+  size_t acc, flags, total;
 };
 
-Layout layout_of(int64_t num_q, int64_t stride) {
+Layout layout_of(int64_t num_q, int64_t stride, int32_t pt_stride) {
   Layout L;
   size_t off = 0;
-  L.la = off;
-  off += round256(static_cast<size_t>(num_q) * stride * 4);
   L.acc = off;
   off += round256(static_cast<size_t>(num_q) * stride * 4);
+  L.flags = off;
+  off += round256(static_cast<size_t>(num_q) * pt_stride);
   L.total = off;
   return L;
 }
@@ -61,59 +69,53 @@ __device__ __forceinline__ int64_t row_len(const Rows& R, int32_t b) {
   return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
-// acc = layer 0 ? s : combine(acc, s), s = sigmoid(la), for the visible
-// positions of row blockIdx.x (blockIdx.y strides over the positions). A
-// position on a page this layer's page table maps out of range was not scored
-// (the scorer flags it); it counts 0 in this layer.
-__global__ void combine_kernel(const float* la, float* acc, int64_t stride, Rows R,
-                               const int32_t* page_table, int64_t num_pages, int layer, int ensemble) {
+// Row blockIdx.x, pages [64 w, 64 w + 64) with w = blockIdx.y: the ensemble
+// score e, keep = e >= threshold or n < sink or n >= L - recent, and a flag per
+// page that holds a kept chunk.
+__global__ void __launch_bounds__(kWinThreads) keep_kernel(const float* acc, int64_t stride, Rows R, int n_layers,
+                                                           int ensemble, float threshold, int32_t sink,
+                                                           int32_t recent, uint8_t* keep, float* scores,
+                                                           uint8_t* flags) {
+  __shared__ uint32_t pflag[kWinPages];
   const int32_t b = blockIdx.x;
   const int64_t L = row_len(R, b);
-  if (L == 0) return;
-  const int32_t* pt = page_table + static_cast<int64_t>(row_req(R, b)) * R.pt_stride;
-  for (int64_t n = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x; n < L;
-       n += static_cast<int64_t>(gridDim.y) * blockDim.x) {
+  const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kWinPages * kPage;
+  if (n0 >= L) return;  // uniform
+  const int64_t n1 = n0 + kWinPages * kPage < L ? n0 + kWinPages * kPage : L;
+  if (threadIdx.x < kWinPages) pflag[threadIdx.x] = 0;
+  __syncthreads();
+  const float inv_layers = 1.0f / static_cast<float>(n_layers);
+  for (int64_t n = n0 + threadIdx.x; n < n1; n += kWinThreads) {
     const int64_t o = static_cast<int64_t>(b) * stride + n;
-    const int32_t phys = pt[n / kPage];
-    const float s = phys < 0 || phys >= num_pages ? 0.0f : 1.0f / (1.0f + expf(-la[o]));
-    acc[o] = layer == 0 ? s : (ensemble == CSA_ENSEMBLE_MAX ? fmaxf(acc[o], s) : acc[o] + s);
+    const float e = ensemble == CSA_ENSEMBLE_MEAN ? acc[o] * inv_layers : acc[o];
+    const bool k = e >= threshold || n < sink || n >= L - recent;
+    keep[o] = k ? 1 : 0;
+    if (scores) scores[o] = e;
+    if (k) pflag[(n - n0) / kPage] = 1;  // several threads may write the same 1
   }
+  __syncthreads();
+  const int64_t p = n0 / kPage + threadIdx.x;
+  if (threadIdx.x < kWinPages && p * kPage < L)
+    flags[static_cast<int64_t>(b) * R.pt_stride + p] = static_cast<uint8_t>(pflag[threadIdx.x]);
 }
 
-// One CTA per row: the combined score, the keep decision and the ascending list
-// of pages with a kept chunk, a window of 256 pages at a time.
-__global__ void __launch_bounds__(kFinalThreads) select_kernel(const float* acc, int64_t stride, Rows R, int n_layers,
-                                                               int ensemble, float threshold, int32_t sink,
-                                                               int32_t recent, uint8_t* keep, float* scores,
-                                                               int32_t* pages, int32_t pages_stride,
-                                                               int32_t* n_pages) {
-  __shared__ uint8_t any[kFinalThreads];
-  __shared__ int32_t warp_count[kFinalThreads / 32];
+// One CTA per row: the ascending list of flagged pages, kListThreads pages at a
+// time (a ballot scan per pass).
+__global__ void __launch_bounds__(kListThreads) list_kernel(const uint8_t* flags, Rows R, int32_t* pages,
+                                                            int32_t pages_stride, int32_t* n_pages) {
+  __shared__ int32_t warp_count[kListThreads / 32];
   const int32_t b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t L = row_len(R, b);
   const int64_t npages = (L + kPage - 1) / kPage;
-  const float inv_layers = 1.0f / static_cast<float>(n_layers);
   int32_t listed = 0;  // uniform
-  for (int64_t p0 = 0; p0 < npages; p0 += kFinalThreads) {
-    any[tid] = 0;
-    __syncthreads();
-    const int64_t n1 = (p0 + kFinalThreads) * kPage < L ? (p0 + kFinalThreads) * kPage : L;
-    for (int64_t n = p0 * kPage + tid; n < n1; n += kFinalThreads) {
-      const int64_t o = static_cast<int64_t>(b) * stride + n;
-      const float e = ensemble == CSA_ENSEMBLE_MEAN ? acc[o] * inv_layers : acc[o];
-      const bool k = e >= threshold || n < sink || n >= L - recent;
-      keep[o] = k ? 1 : 0;
-      if (scores) scores[o] = e;
-      if (k) any[(n / kPage) - p0] = 1;  // several threads may write the same 1
-    }
-    __syncthreads();
-    const bool f = p0 + tid < npages && any[tid] != 0;
+  for (int64_t p0 = 0; p0 < npages; p0 += kListThreads) {
+    const bool f = p0 + tid < npages && flags[static_cast<int64_t>(b) * R.pt_stride + p0 + tid] != 0;
     const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, f);
     if (lane == 0) warp_count[warp] = __popc(ballot);
     __syncthreads();
     int32_t before = listed, total = 0;
-    for (int w = 0; w < kFinalThreads / 32; ++w) {
+    for (int w = 0; w < kListThreads / 32; ++w) {
       if (w < warp) before += warp_count[w];
       total += warp_count[w];
     }
@@ -134,8 +136,8 @@ bool same_rows(const csa_index_args& a, const csa_index_args& b) {
 }  // namespace
 
 extern "C" size_t csa_recall_workspace_bytes(const csa_recall_args* a) {
-  if (!a || !a->layers || a->keep_stride < 0 || a->layers[0].num_q < 0) return 0;
-  return layout_of(a->layers[0].num_q, a->keep_stride).total;
+  if (!a || !a->layers || a->keep_stride < 0 || a->layers[0].num_q < 0 || a->layers[0].pt_stride < 0) return 0;
+  return layout_of(a->layers[0].num_q, a->keep_stride, a->layers[0].pt_stride).total;
 }
 
 extern "C" csa_status csa_recall_level1(const csa_recall_args* a, void* ws, size_t ws_bytes, void* stream) {
@@ -157,34 +159,28 @@ extern "C" csa_status csa_recall_level1(const csa_recall_args* a, void* ws, size
   if ((reinterpret_cast<uintptr_t>(a->pages) & 3) || (reinterpret_cast<uintptr_t>(a->n_pages) & 3) ||
       (a->scores && (reinterpret_cast<uintptr_t>(a->scores) & 3)))
     return CSA_ERR_ALIGNMENT;
-  const Layout W = layout_of(num_q, a->keep_stride);
+  const Layout W = layout_of(num_q, a->keep_stride, L0.pt_stride);
   if (!ws || ws_bytes < W.total) return CSA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) & 255) return CSA_ERR_ALIGNMENT;
   uint8_t* base = static_cast<uint8_t*>(ws);
-  float* la = reinterpret_cast<float*>(base + W.la);
   float* acc = reinterpret_cast<float*>(base + W.acc);
+  uint8_t* flags = base + W.flags;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Rows R{L0.q_len, L0.q_req, L0.num_req, L0.pt_stride};
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return CSA_ERR_CUDA;
+  if (cudaMemsetAsync(acc, 0, static_cast<size_t>(num_q) * a->keep_stride * 4, s) != cudaSuccess) return CSA_ERR_CUDA;
+  const int fold = a->ensemble == CSA_ENSEMBLE_MAX ? CSA_FOLD_MAX : CSA_FOLD_ADD;
   for (int l = 0; l < a->n_layers; ++l) {
-    const csa_index_args& L = a->layers[l];
-    csa_index_args layer = L;
+    csa_index_args layer = a->layers[l];
     layer.q_len = L0.q_len;  // every layer scores layer 0's rows
     layer.q_req = L0.q_req;
     layer.dev_status = L0.dev_status;
-    const csa_status st = csa_index_logits(&layer, la, a->keep_stride, stream);
+    const csa_status st = csa_score_fold(&layer, acc, a->keep_stride, fold, stream);
     if (st != CSA_OK) return st;
-    int64_t gy = (static_cast<int64_t>(sms) * 8 + num_q - 1) / num_q;  // about 8 CTAs per SM in all
-    gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
-    combine_kernel<<<dim3(static_cast<unsigned>(num_q), static_cast<unsigned>(gy)), 256, 0, s>>>(
-        la, acc, a->keep_stride, R, L.page_table, L.num_pages, l, a->ensemble);
-    if (cudaGetLastError() != cudaSuccess) return CSA_ERR_CUDA;
   }
-  select_kernel<<<static_cast<unsigned>(num_q), kFinalThreads, 0, s>>>(
-      acc, a->keep_stride, R, a->n_layers, a->ensemble, a->threshold, a->sink, a->recent, a->keep, a->scores,
-      a->pages, a->pages_stride, a->n_pages);
+  const unsigned windows = static_cast<unsigned>((L0.pt_stride + kWinPages - 1) / kWinPages);
+  keep_kernel<<<dim3(static_cast<unsigned>(num_q), windows), kWinThreads, 0, s>>>(
+      acc, a->keep_stride, R, a->n_layers, a->ensemble, a->threshold, a->sink, a->recent, a->keep, a->scores, flags);
+  if (cudaGetLastError() != cudaSuccess) return CSA_ERR_CUDA;
+  list_kernel<<<static_cast<unsigned>(num_q), kListThreads, 0, s>>>(flags, R, a->pages, a->pages_stride, a->n_pages);
   return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
