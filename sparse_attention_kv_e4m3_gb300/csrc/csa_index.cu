@@ -911,22 +911,34 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
     return fabsf(s) * (((a0[0] + a0[4]) + (a0[1] + a0[5])) + ((a0[2] + a0[6]) + (a0[3] + a0[7])));
   };
 
+  // Sub-staged accumulators: the first sub-tile's logit, read and its stage freed
+  // before the next own tile is loaded (the next tile's MMA waits for this stage).
+  auto first_half = [&](int64_t i, uint32_t sc0, int seg) -> float {
+    tc_fence_after();
+    const int td = static_cast<int>((kSub * i) % kDStages);
+    const float l = logit_one(td, sc0, seg);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
+    return l;
+  };
+
   // Epilogue of own tile i of row b, local tile lt, segment `seg`; the caller
   // has seen the tile's accumulator complete.
   auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, const uint32_t (&sc)[kSub],
-                      const uint32_t (&pos)[kSub]) -> bool {
+                      const uint32_t (&pos)[kSub], float logit0) -> bool {
     tc_fence_after();
     float logit[kSub];
     if constexpr (Geo<H>::kSubStaged) {
-#pragma unroll
-      for (int sub = 0; sub < kSub; ++sub) {  // each stage is freed as soon as it is read
-        const int td = static_cast<int>((kSub * i + sub) % kDStages);
-        logit[sub] = logit_one(td, sc[sub], seg);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
-      }
+      static_assert(kSub == 2, "first_half reads sub-tile 0, this sub-tile 1");
+      logit[0] = logit0;
+      const int td = static_cast<int>((kSub * i + 1) % kDStages);
+      logit[1] = logit_one(td, sc[1], seg);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.dempty[td]));
     } else {
+      (void)logit0;
       const int td = static_cast<int>(i % kDStages);
       logits_of(td, sc, seg, logit);
       tc_fence_before();
@@ -994,11 +1006,13 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
       const bool okd = mbar_wait(smem_u32(&S.dfull[t % kDSignals]), static_cast<uint32_t>((t / kDSignals) & 1),
                                  &S.abort_flag);
       if (!__all_sync(0xFFFFFFFFu, okd)) break;
+      float logit0 = 0.0f;
+      if constexpr (Geo<H>::kSubStaged) logit0 = first_half(t, cur_sc[0], seg);
       if (t + kWorkerGroups < nt) {
         ok = load(t + kWorkerGroups, nxt_sc, nxt_pos);
         if (!ok) break;
       }
-      ok = epilogue(t, cur.b, cur.lt, seg, cur_sc, cur_pos);
+      ok = epilogue(t, cur.b, cur.lt, seg, cur_sc, cur_pos, logit0);
 #pragma unroll
       for (int u = 0; u < kSub; ++u) {
         cur_sc[u] = nxt_sc[u];
