@@ -162,7 +162,8 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
 /*
  * csa_index_score writing the logits themselves (sum_h relu(k . q_h) * fused_w_h, before
  * the sigmoid), in the same layout, with the same arguments and errors (64 or 128 heads).
- * For callers that combine scorers before or after the sigmoid (the Level-1 recall).
+ * For callers that combine the relu'd, head-weighted sums of several scorers before the
+ * sigmoid.
  */
 csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t stride, void* stream);
 
