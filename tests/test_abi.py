@@ -221,3 +221,19 @@ def test_recall_rejects_bad_args(lib):
     assert need > 0
     assert lib.csa_recall_level1(ctypes.byref(native.RecallArgs(**base)), ctypes.c_void_p(0x90000), need - 1,
                                  None) == 4
+
+
+def test_recall_workspace_bytes_arithmetic(lib):
+    """The combined-score plane (num_q x keep_stride fp32) and one flag per row and
+    logical page, each rounded up to 256 bytes; 0 for nonsense sizes."""
+    def ws(num_q, stride, pts):
+        layer = _fake_args(num_q=num_q, pt_stride=pts, num_heads=128)
+        arr = (native.Args * 1)(layer)
+        ra = native.RecallArgs(layers=ctypes.addressof(arr), n_layers=1, keep_stride=stride, pages_stride=pts)
+        return lib.csa_recall_workspace_bytes(ctypes.byref(ra))
+
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for num_q, stride, pts in ((1, 64, 1), (3, 5056, 79), (64, 131072, 2048), (4096, 1 << 14, 256)):
+        assert ws(num_q, stride, pts) == r256(num_q * stride * 4) + r256(num_q * pts)
+    assert ws(-1, 64, 1) == 0 and ws(2, -5, 1) == 0
+    assert lib.csa_recall_workspace_bytes(None) == 0
