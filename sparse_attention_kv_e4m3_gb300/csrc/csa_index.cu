@@ -269,47 +269,76 @@ __device__ PageInfo page_of(const Params& P, int32_t b, int64_t lt, int j, int32
 
 // ------------------------------------------------------------------ planning
 
+// The CTAs split the rows' tiles in row order into contiguous ranges of equal
+// cost. When rows are long (at least kLongRowTiles tiles on average), each row
+// that has tiles also costs kSegTiles "virtual" tiles placed before its first
+// tile, so that a CTA pays for every row it starts (the selection of a new
+// segment starts from nothing: every key passes until the segment has seen k
+// of them): measured on this GPU, a second segment cost a CTA three to five
+// tiles of time, and without the charge the CTAs that cross a row boundary
+// finished last. Batches of short rows (chunked prefill) keep the plain split:
+// there the charge made a few CTAs several times slower, for reasons not yet
+// understood.
+constexpr int64_t kSegTiles = 4, kLongRowTiles = 16;
+
 struct Plan {
-  int64_t total;   // tiles of all rows
-  int64_t t0;      // first tile of this CTA
-  int64_t ntiles;  // tiles of this CTA
-  int64_t lt0;     // local tile of row b0 at t0
-  int32_t b0;      // row holding tile t0
+  int64_t total;   // virtual tiles of all rows
+  int64_t t0;      // first virtual tile of this CTA
+  int64_t ntiles;  // tiles of this CTA (real ones)
+  int64_t lt0;     // local tile of row b0 where the CTA starts
+  int32_t b0;      // row of the CTA's first tile
   int32_t flags;
+  int64_t r0, r1;  // real tiles before virtual tiles t0 and t0 + share (planning scratch)
 };
 
-// Block-wide: tiles of every row, their running sum, and this CTA's share.
-// CTA 0 also writes the exclusive prefix sums (tile_off[num_q + 1]) when given.
+// Block-wide: virtual tiles of every row, their running sum, and this CTA's
+// share of the real tiles. CTA 0 also writes, when given, the exclusive prefix
+// sums of the virtual tiles (tile_off[0 .. num_q]) and the charge per row W
+// (tile_off[num_q + 1]): row b's tiles are virtual tiles tile_off[b] + W ..
+// tile_off[b + 1] - 1.
 template <int NT>
 __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32_t* tile_off) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
   int32_t flags = 0;
-  // pass 1: total
+  // sums of (non-empty rows << 48) | tiles (one scan gives both; tile sums stay far below 2^48)
+  constexpr int64_t kLow = (int64_t{1} << 48) - 1;
+  // pass 1: real tiles and non-empty rows, hence the charge per row and the virtual total
   int64_t part = 0;
-  for (int32_t b = tid; b < P.num_q; b += NT) part += query_tiles(P, b, &flags);
+  for (int32_t b = tid; b < P.num_q; b += NT) {
+    const int64_t t = query_tiles(P, b, &flags);
+    part += t | (t > 0 ? int64_t{1} << 48 : 0);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
   if (lane == 0) warp_sums[warp] = part;
   __syncthreads();
-  int64_t total = 0;
-  for (int i = 0; i < NW; ++i) total += warp_sums[i];
+  int64_t packed_total = 0;
+  for (int i = 0; i < NW; ++i) packed_total += warp_sums[i];
   __syncthreads();
+  const int64_t real_total = packed_total & kLow, rows = packed_total >> 48;
+  const int64_t W = real_total >= kLongRowTiles * rows ? kSegTiles : 0;
+  const int64_t total = real_total + W * rows;
   const int64_t t0 = cta_begin(blockIdx.x, total, gridDim.x);
   const int64_t t1 = cta_begin(blockIdx.x + 1, total, gridDim.x);
   if (tid == 0) {
     plan->total = total;
     plan->t0 = t0;
-    plan->ntiles = t1 - t0;
+    plan->ntiles = 0;
     plan->b0 = P.num_q;
     plan->lt0 = 0;
+    plan->r0 = -1;
+    plan->r1 = t1 >= total ? -2 : -1;  // -2: the range runs to the last tile
   }
-  // pass 2: ordered prefix sums, chunk by chunk
+  __syncthreads();
+  // pass 2: ordered prefix sums of the packed virtual tiles, chunk by chunk; real
+  // tiles before virtual position x inside row b: real_before(b) + max(0, x - vstart(b) - W)
   const bool write_off = tile_off != nullptr && blockIdx.x == 0;
   int64_t running = 0;
   for (int32_t base = 0; base < P.num_q; base += NT) {
     const int32_t b = base + tid;
-    const int64_t t = b < P.num_q ? query_tiles(P, b) : 0;
+    const int64_t tr = b < P.num_q ? query_tiles(P, b) : 0;
+    const int64_t t = tr > 0 ? (tr + W) | (int64_t{1} << 48) : 0;
     int64_t incl = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -323,18 +352,36 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
     for (int i = 0; i < warp; ++i) before += warp_sums[i];
     int64_t chunk = 0;
     for (int i = 0; i < NW; ++i) chunk += warp_sums[i];
-    const int64_t excl = before + incl - t;
+    const int64_t excl_packed = before + incl - t;
+    const int64_t excl = excl_packed & kLow, v = t & kLow;
+    const int64_t real_before = excl - W * (excl_packed >> 48);
     if (b < P.num_q) {
       if (write_off) tile_off[b] = static_cast<int32_t>(excl);
-      if (t > 0 && excl <= t0 && t0 < excl + t) {
+      if (v > 0 && excl <= t0 && t0 < excl + v) {  // the row holding t0 (one thread)
+        const int64_t lt = t0 - excl - W;
         plan->b0 = b;
-        plan->lt0 = t0 - excl;
+        plan->lt0 = lt > 0 ? lt : 0;
+        plan->r0 = real_before + (lt > 0 ? lt : 0);
+      }
+      if (v > 0 && excl <= t1 && t1 < excl + v) {  // the row holding t1 (one thread)
+        const int64_t lt = t1 - excl - W;
+        plan->r1 = real_before + (lt > 0 ? lt : 0);
       }
     }
     running += chunk;
-    if (!write_off && running > t0) break;  // uniform: every thread sees the same running sum
+    if (!write_off && (running & kLow) > t1) break;  // uniform: every thread sees the same running sum
   }
-  if (write_off && tid == 0) tile_off[P.num_q] = static_cast<int32_t>(total);
+  __syncthreads();
+  if (tid == 0) {
+    // a range that runs to the last tile ends after every real tile; the loop did not
+    // stop early then, so `running` holds the whole packed sum
+    const int64_t r1 = plan->r1 == -2 ? (running & kLow) - W * (running >> 48) : plan->r1;
+    plan->ntiles = (plan->r0 >= 0 && r1 > plan->r0) ? r1 - plan->r0 : 0;
+  }
+  if (write_off && tid == 0) {
+    tile_off[P.num_q] = static_cast<int32_t>(total);
+    tile_off[P.num_q + 1] = static_cast<int32_t>(W);
+  }
   if (flags) atomicOr(&plan->flags, flags);
   __syncthreads();
 }
@@ -1204,10 +1251,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
     S.sel.n = 0;
     S.sel.tau = 0;
   }
-  const int64_t t0 = tile_off[b], t1 = tile_off[b + 1], total = tile_off[P.num_q];
+  // row b's tiles are virtual tiles t0 + W .. t1 - 1 (none when t0 == t1)
+  const int64_t t0 = tile_off[b], t1 = tile_off[b + 1], total = tile_off[P.num_q], W = tile_off[P.num_q + 1];
   int64_t c0 = 0, c1 = -1;
   if (t0 < t1) {
-    c0 = cta_of(t0, total, P.grid);
+    c0 = cta_of(t0 + W, total, P.grid);
     c1 = cta_of(t1 - 1, total, P.grid);
   }
   const int nslots = static_cast<int>(c1 - c0 + 1);  // 0 for an empty row
@@ -1398,7 +1446,8 @@ int g_sms[kMaxDevices];
 bool g_ready[kMaxDevices];
 
 size_t slot_bytes_for(int32_t k) { return (16 + 8 * static_cast<size_t>(loose_keep(k)) + 15) & ~size_t(15); }
-size_t slots_offset_for(int32_t num_q) { return (4 * (static_cast<size_t>(num_q) + 1) + 255) & ~size_t(255); }
+// tile_off[num_q + 2] (virtual prefix sums and the charge per row), then the slots
+size_t slots_offset_for(int32_t num_q) { return (4 * (static_cast<size_t>(num_q) + 2) + 255) & ~size_t(255); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
