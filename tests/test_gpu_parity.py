@@ -93,6 +93,9 @@ SMALL = {
                          q_len=lambda h, n: np.minimum(3000, np.arange(n) * 70 + 1), seed=34),
     "padded_pages": dict(num_q=2, history=[1500, 900], page_pad=112, seed=35),
     "contiguous": dict(num_q=2, history=[4096, 4000], shuffle=False, seed=36),
+    # long rows on average (the plan charges each row start extra tiles) mixed with
+    # empty and one-tile rows, so that some CTA ranges hold only a row's charge
+    "charged_split": dict(num_q=7, history=[20000, 0, 256, 0, 50000, 64, 4096], seed=37),
 }
 
 
