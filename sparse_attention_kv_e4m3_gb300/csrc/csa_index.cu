@@ -301,13 +301,15 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
   int32_t flags = 0;
-  // sums of (non-empty rows << 48) | tiles (one scan gives both; tile sums stay far below 2^48)
-  constexpr int64_t kLow = (int64_t{1} << 48) - 1;
+  // sums of (non-empty rows << 32) | tiles: one scan gives both (tile sums, like
+  // tile_off, stay below 2^31; row counts below 2^31)
+  constexpr int kShift = 32;
+  constexpr int64_t kLow = (int64_t{1} << kShift) - 1;
   // pass 1: real tiles and non-empty rows, hence the charge per row and the virtual total
   int64_t part = 0;
   for (int32_t b = tid; b < P.num_q; b += NT) {
     const int64_t t = query_tiles(P, b, &flags);
-    part += t | (t > 0 ? int64_t{1} << 48 : 0);
+    part += t | (t > 0 ? int64_t{1} << kShift : 0);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
@@ -316,7 +318,7 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
   int64_t packed_total = 0;
   for (int i = 0; i < NW; ++i) packed_total += warp_sums[i];
   __syncthreads();
-  const int64_t real_total = packed_total & kLow, rows = packed_total >> 48;
+  const int64_t real_total = packed_total & kLow, rows = packed_total >> kShift;
   const int64_t W = real_total >= kLongRowTiles * rows ? kSegTiles : 0;
   const int64_t total = real_total + W * rows;
   const int64_t t0 = cta_begin(blockIdx.x, total, gridDim.x);
@@ -338,7 +340,7 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
   for (int32_t base = 0; base < P.num_q; base += NT) {
     const int32_t b = base + tid;
     const int64_t tr = b < P.num_q ? query_tiles(P, b) : 0;
-    const int64_t t = tr > 0 ? (tr + W) | (int64_t{1} << 48) : 0;
+    const int64_t t = tr > 0 ? (tr + W) | (int64_t{1} << kShift) : 0;
     int64_t incl = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -354,7 +356,7 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
     for (int i = 0; i < NW; ++i) chunk += warp_sums[i];
     const int64_t excl_packed = before + incl - t;
     const int64_t excl = excl_packed & kLow, v = t & kLow;
-    const int64_t real_before = excl - W * (excl_packed >> 48);
+    const int64_t real_before = excl - W * (excl_packed >> kShift);
     if (b < P.num_q) {
       if (write_off) tile_off[b] = static_cast<int32_t>(excl);
       if (v > 0 && excl <= t0 && t0 < excl + v) {  // the row holding t0 (one thread)
@@ -375,7 +377,7 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
   if (tid == 0) {
     // a range that runs to the last tile ends after every real tile; the loop did not
     // stop early then, so `running` holds the whole packed sum
-    const int64_t r1 = plan->r1 == -2 ? (running & kLow) - W * (running >> 48) : plan->r1;
+    const int64_t r1 = plan->r1 == -2 ? (running & kLow) - W * (running >> kShift) : plan->r1;
     plan->ntiles = (plan->r0 >= 0 && r1 > plan->r0) ? r1 - plan->r0 : 0;
   }
   if (write_off && tid == 0) {
