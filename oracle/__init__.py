@@ -108,6 +108,22 @@ def _bind(path: str):
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int32, ctypes.c_void_p]
     lib.oracle_recall.restype = ctypes.c_int32
+    lib.oracle_e2m1.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1.restype = ctypes.c_double
+    lib.oracle_ue8m0.argtypes = [ctypes.c_uint8]
+    lib.oracle_ue8m0.restype = ctypes.c_double
+    lib.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+    lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+    lib.oracle_mxfp4_block.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_mxfp4_block.restype = None
+    lib.oracle_mxfp4_round.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    lib.oracle_mxfp4_round.restype = None
+    lib.oracle_fp4_record.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_fp4_record.restype = None
+    lib.oracle_fp4_decode.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_fp4_decode.restype = None
+    lib.oracle_fp4_logit.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    lib.oracle_fp4_logit.restype = ctypes.c_double
     return lib
 
 
@@ -209,6 +225,30 @@ class Oracle:
 
     def recall(self, layers, mean: bool, threshold: float, sink: int, recent: int):
         return _recall(self.lib, layers, mean, threshold, sink, recent)
+
+    def e2m1(self, code: int) -> float:
+        return float(self.lib.oracle_e2m1(int(code)))
+
+    def ue8m0(self, byte: int) -> float:
+        return float(self.lib.oracle_ue8m0(int(byte)))
+
+    def e2m1_encode(self, v: float) -> int:
+        return int(self.lib.oracle_e2m1_encode(float(v)))
+
+    def mxfp4_block(self, x):
+        return _mxfp4_block(self.lib, x)
+
+    def mxfp4_round(self, x):
+        return _mxfp4_round(self.lib, x)
+
+    def fp4_record(self, x):
+        return _fp4_record(self.lib, x)
+
+    def fp4_decode(self, rec):
+        return _fp4_decode(self.lib, rec)
+
+    def fp4_logit(self, rec, q_bits, w):
+        return _fp4_logit(self.lib, rec, q_bits, w)
 
 
 def load_build(path: str) -> Oracle:
@@ -369,3 +409,79 @@ def _recall(lib, layers, mean: bool, threshold: float, sink: int, recent: int):
 
 def recall(layers, mean: bool, threshold: float, sink: int, recent: int):
     return _recall(_load(), layers, mean, threshold, sink, recent)
+
+
+# ------------------------------------------------------------------ FP4 (MXFP4) variant
+
+def _mxfp4_block(lib, x):
+    """32 values -> (32 e2m1 codes, one per byte; the UE8M0 scale byte)."""
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    assert v.shape == (32,)
+    codes = np.zeros(32, dtype=np.uint8)
+    sc = ctypes.c_uint8(0)
+    lib.oracle_mxfp4_block(v.ctypes.data, codes.ctypes.data, ctypes.byref(sc))
+    return codes, int(sc.value)
+
+
+def _mxfp4_round(lib, x):
+    """Values (length a multiple of 32) MXFP4-rounded block by block, as fp64."""
+    v = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    assert v.size % 32 == 0
+    out = np.zeros(v.size, dtype=np.float64)
+    lib.oracle_mxfp4_round(v.ctypes.data, int(v.size), out.ctypes.data)
+    return out
+
+
+def _fp4_record(lib, x):
+    """A key row of 128 values -> its 68-byte FP4 record."""
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    assert v.shape == (128,)
+    rec = np.zeros(68, dtype=np.uint8)
+    lib.oracle_fp4_record(v.ctypes.data, rec.ctypes.data)
+    return rec
+
+
+def _fp4_decode(lib, rec):
+    r = np.ascontiguousarray(rec, dtype=np.uint8)
+    assert r.shape == (68,)
+    k = np.zeros(128, dtype=np.float64)
+    lib.oracle_fp4_decode(r.ctypes.data, k.ctypes.data)
+    return k
+
+
+def _fp4_logit(lib, rec, q_bits, w):
+    """Logit of a 68-byte FP4 key record against q (bf16 bit patterns [H, 128]) and
+    head weights w [H]; both sides MXFP4-rounded."""
+    r = np.ascontiguousarray(rec, dtype=np.uint8)
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    wv = np.ascontiguousarray(w, dtype=np.float32)
+    assert r.shape == (68,) and q.ndim == 2 and q.shape[1] == 128 and wv.shape == (q.shape[0],)
+    return float(lib.oracle_fp4_logit(r.ctypes.data, q.ctypes.data, wv.ctypes.data, int(q.shape[0])))
+
+
+def e2m1(code: int) -> float:
+    return Oracle().e2m1(code)
+
+
+def e2m1_encode(v: float) -> int:
+    return Oracle().e2m1_encode(v)
+
+
+def mxfp4_block(x):
+    return _mxfp4_block(_load(), x)
+
+
+def mxfp4_round(x):
+    return _mxfp4_round(_load(), x)
+
+
+def fp4_record(x):
+    return _fp4_record(_load(), x)
+
+
+def fp4_decode(rec):
+    return _fp4_decode(_load(), rec)
+
+
+def fp4_logit(rec, q_bits, w):
+    return _fp4_logit(_load(), rec, q_bits, w)

@@ -533,3 +533,114 @@ int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t en
   free(len);
   return flags;
 }
+
+/* ------------------------------------------------------------------ FP4 (MXFP4) variant
+ *
+ * BatchGen #153 commit log (the indexer quantisation notes) and the V4.1 runtime
+ * page: the published model FP4-rounds the index query and key alike (e2m1,
+ * "MXFP4", cvt.e2m1x2) before the index score. The pages name the element type
+ * and MXFP4 but print neither the block size nor a record layout. Readings
+ * (also listed in the design doc), following the OCP MX format for MXFP4:
+ *   - blocks of 32 consecutive elements along head_dim share one UE8M0 scale
+ *     X = 2^(floor(log2(amax)) - 2), 2 being the largest e2m1 exponent; the
+ *     exponent is clamped to [-127, 127]; a block of zeros takes X = 2^-127;
+ *   - an element is stored as the nearest e2m1 value of x / X, ties to the even
+ *     mantissa, magnitudes past 6 saturating to 6;
+ *   - a key record is 64 bytes of codes (element 2j in the low nibble of byte j)
+ *     followed by the 4 UE8M0 bytes of its blocks, 68 bytes; 64 records a page.
+ * The logit is the indexer's, on the dequantised values:
+ *   logit = sum_h relu(k . q_h) * w_h, with k and q_h both MXFP4-rounded.
+ */
+#define OR_FP4_BLOCK 32
+#define OR_FP4_REC_BYTES (OR_D / 2 + OR_D / OR_FP4_BLOCK)
+
+/* e2m1 code (4 bits): sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0;
+ * exponent 0 is subnormal (value = mantissa * 0.5). No infinities or NaNs. */
+double oracle_e2m1(uint8_t code) {
+  const int sign = (code >> 3) & 1, E = (code >> 1) & 3, m = code & 1;
+  const double v = E == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, E - 1);
+  return sign ? -v : v;
+}
+
+/* UE8M0 scale byte: 2^(e - 127); 255 is NaN. */
+double oracle_ue8m0(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+/* Nearest e2m1 code of v (already divided by its block scale): every one of the
+ * 8 magnitudes is tried; the closer wins, a tie goes to the even mantissa;
+ * magnitudes at or past 6 saturate. */
+uint8_t oracle_e2m1_encode(double v) {
+  const uint8_t sign = (v < 0 || (v == 0 && signbit(v))) ? 8 : 0;
+  const double a = fabs(v);
+  if (a >= 6.0) return sign | 7;
+  uint8_t best = 0;
+  double best_d = INFINITY;
+  for (uint8_t c = 0; c < 8; ++c) {
+    const double d = fabs(oracle_e2m1(c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | best;
+}
+
+/* One block of 32 values: its UE8M0 scale byte and 32 codes (one per byte). */
+void oracle_mxfp4_block(const float* x, uint8_t* codes, uint8_t* scale) {
+  double amax = 0.0;
+  for (int i = 0; i < OR_FP4_BLOCK; ++i) amax = fmax(amax, fabs((double)x[i]));
+  int e = -127;
+  if (amax > 0.0) {
+    int E2;
+    (void)frexp(amax, &E2); /* amax = f * 2^E2, f in [0.5, 1): floor(log2 amax) = E2 - 1 */
+    e = (E2 - 1) - 2;
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+  }
+  *scale = (uint8_t)(e + 127);
+  const double X = ldexp(1.0, e);
+  for (int i = 0; i < OR_FP4_BLOCK; ++i) codes[i] = oracle_e2m1_encode((double)x[i] / X);
+}
+
+/* n values (n a multiple of 32) quantised and dequantised block by block. */
+void oracle_mxfp4_round(const float* x, int64_t n, double* out) {
+  uint8_t codes[OR_FP4_BLOCK], sc;
+  for (int64_t b = 0; b + OR_FP4_BLOCK <= n; b += OR_FP4_BLOCK) {
+    oracle_mxfp4_block(x + b, codes, &sc);
+    for (int i = 0; i < OR_FP4_BLOCK; ++i) out[b + i] = oracle_e2m1(codes[i]) * oracle_ue8m0(sc);
+  }
+}
+
+/* A key row of 128 values as a 68-byte FP4 record. */
+void oracle_fp4_record(const float* x, uint8_t* rec) {
+  uint8_t codes[OR_D];
+  for (int blk = 0; blk < OR_D / OR_FP4_BLOCK; ++blk)
+    oracle_mxfp4_block(x + blk * OR_FP4_BLOCK, codes + blk * OR_FP4_BLOCK, rec + OR_D / 2 + blk);
+  for (int j = 0; j < OR_D / 2; ++j) rec[j] = (uint8_t)((codes[2 * j] & 15) | ((codes[2 * j + 1] & 15) << 4));
+}
+
+/* The 128 key values a 68-byte FP4 record holds. */
+void oracle_fp4_decode(const uint8_t* rec, double* k) {
+  for (int d = 0; d < OR_D; ++d) {
+    const uint8_t code = (uint8_t)((rec[d / 2] >> (4 * (d & 1))) & 15);
+    k[d] = oracle_e2m1(code) * oracle_ue8m0(rec[OR_D / 2 + d / OR_FP4_BLOCK]);
+  }
+}
+
+/* Logit of one FP4 key record against an H-head bf16 query (bit patterns,
+ * [H][128]) and fp32 head weights: both sides MXFP4-rounded, then the indexer's
+ * relu'd, head-weighted sum in fp64. */
+double oracle_fp4_logit(const uint8_t* rec, const uint16_t* q, const float* w, int32_t H) {
+  double k[OR_D];
+  oracle_fp4_decode(rec, k);
+  double logit = 0.0;
+  for (int32_t h = 0; h < H; ++h) {
+    float qf[OR_D];
+    double qr[OR_D];
+    for (int d = 0; d < OR_D; ++d) qf[d] = (float)oracle_bf16(q[(int64_t)h * OR_D + d]);
+    oracle_mxfp4_round(qf, OR_D, qr);
+    double dot = 0.0;
+    for (int d = 0; d < OR_D; ++d) dot += k[d] * qr[d];
+    const double relu = dot > 0.0 ? dot : 0.0;
+    logit += relu * (double)w[h];
+  }
+  return logit;
+}

@@ -609,4 +609,131 @@ def pin_recall_rows_and_unreadable_pages(o: O.Oracle):
     assert not keep[2].any() and len(pages[2]) == 0 and np.all(sc[2] == 0.0)
 
 
+# ---------------------------------------------------------------- FP4 (MXFP4) variant
+
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # OCP FP4 E2M1 magnitudes, codes 0..7
+
+
+def _grid_block(rng, s):
+    """32 values on the e2m1 grid times 2^s, the largest magnitude present."""
+    top = float(rng.choice(E2M1_VALUES[1:]))
+    mags = rng.choice([g for g in E2M1_VALUES if g <= top], 32)
+    x = mags * rng.choice([-1.0, 1.0], 32) * 2.0 ** s
+    x[int(rng.integers(32))] = top * 2.0 ** s
+    return x.astype(np.float32)
+
+
+def pin_fp4_e2m1_table(o: O.Oracle):
+    """The 16 e2m1 codes decode to the OCP FP4 E2M1 table (sign in bit 3); a UE8M0
+    byte is 2^(e - 127), 255 is NaN."""
+    for c in range(16):
+        want = E2M1_VALUES[c & 7] * (-1.0 if c & 8 else 1.0)
+        got = o.e2m1(c)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (c, got)
+    for e in (0, 1, 100, 126, 127, 128, 254):
+        assert o.ue8m0(e) == 2.0 ** (e - 127)
+    assert math.isnan(o.ue8m0(255))
+
+
+def pin_fp4_encode_nearest_even(o: O.Oracle):
+    """Encoding picks the nearest e2m1 magnitude (brute force over the table), a tie
+    goes to the even code, magnitudes at or past 6 saturate; the seven midpoints."""
+    grid = np.array(E2M1_VALUES)
+    rng = np.random.default_rng(41)
+    for v in list(rng.uniform(-7.0, 7.0, 3000)) + [6.0, 6.5, 1e9, -1e9, 0.0]:
+        c = o.e2m1_encode(v)
+        a = abs(v)
+        if a >= 6.0:
+            assert c & 7 == 7, (v, c)
+        else:
+            d = np.abs(grid - a)
+            best = np.flatnonzero(d == d.min())
+            want = int(best[0]) if len(best) == 1 else int([b for b in best if b % 2 == 0][0])
+            assert c & 7 == want, (v, c, want)
+        assert (c >> 3) == (1 if v < 0 else 0), (v, c)
+    for v, want in ((0.25, 0.0), (0.75, 1.0), (1.25, 1.0), (1.75, 2.0), (2.5, 2.0), (3.5, 4.0), (5.0, 4.0)):
+        assert o.e2m1(o.e2m1_encode(v)) == want and o.e2m1(o.e2m1_encode(-v)) == -want, v
+
+
+def pin_fp4_block_scale(o: O.Oracle):
+    """OCP MX scale X = 2^(floor(log2 amax) - 2): amax in [4, 8) x 2^s gives the scale
+    byte 127 + s, values past 6 X saturate; scaling a block by 2^k adds k to the byte
+    and keeps the codes; a block of zeros has scale byte 0 and zero codes."""
+    rng = np.random.default_rng(42)
+    for s in (-20, -3, 0, 5, 30):
+        x = (rng.uniform(-1.0, 1.0, 32) * 2.0 ** s).astype(np.float32)
+        for top, sat in ((6.0, False), (4.0, False), (7.5, True)):
+            x[7] = np.float32(top * 2.0 ** s)
+            codes, sc = o.mxfp4_block(x)
+            assert sc == 127 + s, (s, top, sc)
+            assert (codes[7] == 7) if sat else (o.e2m1(int(codes[7])) == top), (s, top, codes[7])
+            c2, sc2 = o.mxfp4_block((x * np.float32(8.0)).astype(np.float32))
+            assert sc2 == sc + 3 and np.array_equal(c2, codes)
+        x[7] = np.float32(3.9 * 2.0 ** s)  # floor(log2 3.9) = 1: X = 2^(s - 1), 7.8 saturates
+        codes, sc = o.mxfp4_block(x)
+        assert sc == 126 + s and codes[7] == 7
+    codes, sc = o.mxfp4_block(np.zeros(32, np.float32))
+    assert sc == 0 and not codes.any()
+
+
+def pin_fp4_grid_round_trip(o: O.Oracle):
+    """Blocks whose values lie on the e2m1 grid times a power of two come back exactly,
+    whatever their largest magnitude (the scale then maps every value onto the grid)."""
+    rng = np.random.default_rng(43)
+    for _ in range(60):
+        x = _grid_block(rng, int(rng.integers(-12, 12)))
+        assert np.array_equal(o.mxfp4_round(x), x.astype(np.float64)), x
+
+
+def pin_fp4_record_layout(o: O.Oracle):
+    """A record is 64 code bytes (element 2j in the low nibble of byte j) then the four
+    block scale bytes; decoding gives the row back when it lies on the grid."""
+    rng = np.random.default_rng(44)
+    x = np.concatenate([_grid_block(rng, s) for s in (-3, 0, 2, 7)])
+    rec = o.fp4_record(x)
+    codes = np.concatenate([o.mxfp4_block(x[32 * b:32 * b + 32])[0] for b in range(4)])
+    for b in range(4):
+        assert rec[64 + b] == o.mxfp4_block(x[32 * b:32 * b + 32])[1]
+    for j in range(64):
+        assert rec[j] == (codes[2 * j] | (codes[2 * j + 1] << 4)), j
+    assert np.array_equal(o.fp4_decode(rec), x.astype(np.float64))
+
+
+def pin_fp4_logit_equals_fp8_indexer(o: O.Oracle):
+    """Keys and queries on the e2m1 grid (times powers of two per block) are exact both
+    as MXFP4 and as e4m3 records with a power-of-two scale / bf16 queries: there the
+    FP4 logit equals the logit of the FP8 indexer (pinned on its own above)."""
+    rng = np.random.default_rng(45)
+    keys = np.stack([np.concatenate([_grid_block(rng, int(rng.integers(-2, 3))) for _ in range(4)])
+                     for _ in range(20)])
+    q = np.stack([np.concatenate([_grid_block(rng, int(rng.integers(-3, 2))) for _ in range(4)])
+                  for _ in range(H)])
+    w = (rng.standard_normal(H) / 8.0).astype(np.float32)
+    scale = 2.0 ** -3
+    recs = np.stack([record({d: e4m3_code(float(keys[i, d]) / scale) for d in range(D)}, scale)
+                     for i in range(keys.shape[0])])
+    P = O.Problem(hand_workload(recs, q, w))
+    qb = bf16_bits(q).reshape(H, D)
+    for i in range(keys.shape[0]):
+        lg8 = o.logit(P, 0, i)
+        lg4 = o.fp4_logit(o.fp4_record(keys[i]), qb, w)
+        assert abs(lg4 - lg8) <= 1e-12 * (1.0 + abs(lg8)), (i, lg4, lg8)
+
+
+def pin_fp4_logit_composes_rounding(o: O.Oracle):
+    """Off the grid: the FP4 logit is the relu'd, head-weighted sum over the decoded key
+    and the block-rounded bf16 query (both pinned above), recomputed here with numpy."""
+    rng = np.random.default_rng(46)
+    for t in range(8):
+        key = (rng.standard_normal(D) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        q = (rng.standard_normal((3, D)) * 10.0 ** rng.uniform(-2, 2)).astype(np.float32)
+        w = rng.standard_normal(3).astype(np.float32)
+        qb = bf16_bits(q).reshape(3, D)
+        qf = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).float().numpy()
+        k = o.fp4_decode(o.fp4_record(key))
+        want = sum(max(0.0, float(k @ o.mxfp4_round(qf[h]))) * float(w[h]) for h in range(3))
+        got = o.fp4_logit(o.fp4_record(key), qb, w)
+        assert abs(got - want) <= 1e-12 * (1.0 + abs(want)), (t, got, want)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -66,6 +66,21 @@ MUTATIONS = [
     ("recall_unreadable_scores_half", "const double sc = valid[o] ? oracle_sigmoid(logit[o]) : 0.0;",
      "const double sc = valid[o] ? oracle_sigmoid(logit[o]) : 0.5;"),
     ("recall_rows_of_each_layer", "    P.q_len = layers[0].q_len;\n    P.q_req = layers[0].q_req;\n", ""),
+    # FP4 (MXFP4) variant
+    ("fp4_emax_1", "    e = (E2 - 1) - 2;", "    e = (E2 - 1) - 1;"),
+    ("fp4_scale_ceil", "    e = (E2 - 1) - 2;", "    e = E2 - 2;"),
+    ("fp4_ties_odd",
+     "const double d = fabs(oracle_e2m1(c) - a);\n    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {",
+     "const double d = fabs(oracle_e2m1(c) - a);\n    if (d < best_d || (d == best_d && (c & 1) == 1 && (best & 1) == 0)) {"),
+    ("fp4_subnormal_quarter", "const double v = E == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, E - 1);",
+     "const double v = E == 0 ? 0.25 * m : ldexp(1.0 + 0.5 * m, E - 1);"),
+    ("fp4_nibbles_swapped", "rec[j] = (uint8_t)((codes[2 * j] & 15) | ((codes[2 * j + 1] & 15) << 4));",
+     "rec[j] = (uint8_t)((codes[2 * j + 1] & 15) | ((codes[2 * j] & 15) << 4));"),
+    ("fp4_decode_block0_scale", "k[d] = oracle_e2m1(code) * oracle_ue8m0(rec[OR_D / 2 + d / OR_FP4_BLOCK]);",
+     "k[d] = oracle_e2m1(code) * oracle_ue8m0(rec[OR_D / 2]);"),
+    ("fp4_query_unrounded", "for (int d = 0; d < OR_D; ++d) dot += k[d] * qr[d];",
+     "for (int d = 0; d < OR_D; ++d) dot += k[d] * qf[d];"),
+    ("fp4_relu_dropped", "const double relu = dot > 0.0 ? dot : 0.0;", "const double relu = dot;"),
 ]
 
 
