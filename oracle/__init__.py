@@ -65,6 +65,7 @@ class _Problem(ctypes.Structure):
         ("resident", ctypes.c_void_p),
         ("n_resident", ctypes.c_void_p),
         ("res_stride", ctypes.c_int32),
+        ("format", ctypes.c_int32),
     ]
 
 
@@ -145,10 +146,14 @@ class Problem:
 
     Takes any object with the attributes of a synthetic workload: q (uint16 bf16
     bits [num_q, H, D]), fused_w, kv ([num_pages, page_stride] uint8),
-    page_table, q_len, q_req, resident, n_resident.
+    page_table, q_len, q_req, resident, n_resident, and the record format
+    ("e4m3" or "mxfp4"; taken from the workload's `record_format` when not given).
     """
 
-    def __init__(self, w):
+    FORMATS = {"e4m3": 0, "mxfp4": 1}
+
+    def __init__(self, w, record_format=None):
+        record_format = record_format or getattr(w, "record_format", "e4m3")
         c = np.ascontiguousarray
         self.q = c(w.q, dtype=np.uint16)
         self.fused_w = c(w.fused_w, dtype=np.float32)
@@ -166,7 +171,7 @@ class Problem:
             _ptr(self.kv), int(self.kv.shape[0]), int(self.kv.shape[1]),
             _ptr(self.page_table), self.num_req, self.pt_stride,
             _ptr(self.q_req), _ptr(self.q_len), _ptr(self.resident), _ptr(self.n_resident),
-            self.res_stride)
+            self.res_stride, self.FORMATS[record_format])
 
     @property
     def ref(self):

@@ -61,7 +61,14 @@ typedef struct oracle_problem {
   const int32_t* resident;    /* NULL = full history */
   const int32_t* n_resident;
   int32_t res_stride;
+  int32_t format;             /* records: 0 = e4m3 + fp32 scale (132 B), 1 = MXFP4 (68 B) */
 } oracle_problem;
+
+/* FP4 (MXFP4) variant, defined in its section at the end of this file. */
+#define OR_FP4_BLOCK 32
+#define OR_FP4_REC_BYTES (OR_D / 2 + OR_D / OR_FP4_BLOCK)
+void oracle_mxfp4_round(const float* x, int64_t n, double* out);
+void oracle_fp4_decode(const uint8_t* rec, double* k);
 
 /* OCP FP8 E4M3 ("fn") byte -> value. E = 0: subnormal m/8 * 2^-6; otherwise
  * (1 + m/8) * 2^(E-7); E = 15 and m = 7 is NaN. */
@@ -179,12 +186,22 @@ int64_t oracle_visible(const oracle_problem* P, int32_t b, int64_t* pos, int64_t
   return n;
 }
 
-/* q of row b decoded to fp64 and stored d-major: qT[d*H + h] = q[b][h][d]. */
+/* q of row b decoded to fp64 and stored d-major: qT[d*H + h] = q[b][h][d]; with
+ * MXFP4 records the query is block-rounded the same way, head by head. */
 static void decode_query(const oracle_problem* P, int32_t b, double* qT) {
   const int H = P->H;
   const uint16_t* qb = P->q + (int64_t)b * H * OR_D;
   for (int h = 0; h < H; ++h)
     for (int d = 0; d < OR_D; ++d) qT[d * H + h] = oracle_bf16(qb[h * OR_D + d]);
+  if (P->format == 1) {
+    for (int h = 0; h < H; ++h) {
+      float qf[OR_D];
+      double qr[OR_D];
+      for (int d = 0; d < OR_D; ++d) qf[d] = (float)qT[d * H + h];
+      oracle_mxfp4_round(qf, OR_D, qr);
+      for (int d = 0; d < OR_D; ++d) qT[d * H + h] = qr[d];
+    }
+  }
 }
 
 /*
@@ -199,14 +216,23 @@ static double logit_at(const oracle_problem* P, int32_t b, const double* qT, int
   int32_t req = P->q_req ? P->q_req[b] : b;
   int64_t p = position / OR_PAGE, r = position % OR_PAGE;
   int32_t phys = P->page_table[(int64_t)req * P->pt_stride + p];
-  const uint8_t* rec = P->kv + (int64_t)phys * P->page_stride + r * OR_REC_BYTES;
-  const double s = oracle_scale(rec);
+  const uint8_t* rec = P->kv + (int64_t)phys * P->page_stride + r * (P->format == 1 ? OR_FP4_REC_BYTES : OR_REC_BYTES);
   double dot[256];
   for (int h = 0; h < H; ++h) dot[h] = 0.0;
-  for (int d = 0; d < OR_D; ++d) {
-    const double kd = oracle_e4m3(rec[d]) * s; /* dequantise: e4m3 value times scale */
-    const double* qd = qT + d * H;
-    for (int h = 0; h < H; ++h) dot[h] += kd * qd[h];
+  if (P->format == 1) {
+    double k[OR_D];
+    oracle_fp4_decode(rec, k); /* dequantise: e2m1 codes times their block scales */
+    for (int d = 0; d < OR_D; ++d) {
+      const double* qd = qT + d * H;
+      for (int h = 0; h < H; ++h) dot[h] += k[d] * qd[h];
+    }
+  } else {
+    const double s = oracle_scale(rec);
+    for (int d = 0; d < OR_D; ++d) {
+      const double kd = oracle_e4m3(rec[d]) * s; /* dequantise: e4m3 value times scale */
+      const double* qd = qT + d * H;
+      for (int h = 0; h < H; ++h) dot[h] += kd * qd[h];
+    }
   }
   double logit = 0.0;
   for (int h = 0; h < H; ++h) {
@@ -551,9 +577,6 @@ int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t en
  * The logit is the indexer's, on the dequantised values:
  *   logit = sum_h relu(k . q_h) * w_h, with k and q_h both MXFP4-rounded.
  */
-#define OR_FP4_BLOCK 32
-#define OR_FP4_REC_BYTES (OR_D / 2 + OR_D / OR_FP4_BLOCK)
-
 /* e2m1 code (4 bits): sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0;
  * exponent 0 is subnormal (value = mantissa * 0.5). No infinities or NaNs. */
 double oracle_e2m1(uint8_t code) {

@@ -40,6 +40,8 @@ RECORD_BYTES = HEAD_DIM + 4
 PAGE_BYTES = PAGE_RECORDS * RECORD_BYTES
 E4M3_MAX = 448.0
 _CHUNK_PAGES = 1024
+FP4_RECORD_BYTES = HEAD_DIM // 2 + HEAD_DIM // 32  # 64 code bytes + 4 block-scale bytes
+FP4_PAGE_BYTES = PAGE_RECORDS * FP4_RECORD_BYTES
 
 
 @dataclass
@@ -56,6 +58,7 @@ class Workload:
     resident: Optional[np.ndarray] = None    # int32 [num_req, res_stride] or None
     n_resident: Optional[np.ndarray] = None  # int32 [num_req] or None
     meta: dict = field(default_factory=dict)
+    record_format: str = "e4m3"              # "e4m3" (132-byte records) or "mxfp4" (68-byte)
 
     @property
     def num_q(self) -> int:
@@ -102,8 +105,9 @@ class Workload:
         return out
 
     def k_bytes(self) -> int:
-        """Bytes of K rows that the visible records occupy (132 per record)."""
-        return int(self.visible_counts().sum()) * RECORD_BYTES
+        """Bytes of K rows that the visible records occupy (132 or 68 per record)."""
+        rec = FP4_RECORD_BYTES if self.record_format == "mxfp4" else RECORD_BYTES
+        return int(self.visible_counts().sum()) * rec
 
 
 def _bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -243,6 +247,23 @@ def level1_layers(w: Workload, n_layers: int, seed: int) -> list:
         out.append(Workload(name=f"{w.name}_l{l}", q=_bf16_bits(q), fused_w=fw.astype(np.float32), kv=w.kv,
                             page_table=w.page_table, q_len=w.q_len, q_req=w.q_req, meta=dict(w.meta, layer=l)))
     return out
+
+
+def mxfp4_cache(w: Workload, seed: int) -> Workload:
+    """The same rows, lengths and page table over an MXFP4 cache (68-byte records:
+    64 bytes of e2m1 codes, element 2j in the low nibble of byte j, then 4 UE8M0
+    block-scale bytes). The records are drawn directly, codes as uniform bytes and
+    scale bytes in [124, 128] (block scales 2^-3 .. 2^1), so nothing is quantised
+    here; from `PCG64(SeedSequence(seed, spawn_key=(9,)))`."""
+    import dataclasses
+
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(9,))))
+    n = w.kv.shape[0]
+    kv = np.zeros((n, FP4_PAGE_BYTES), dtype=np.uint8)
+    recs = kv.reshape(n, PAGE_RECORDS, FP4_RECORD_BYTES)
+    recs[..., :HEAD_DIM // 2] = rng.integers(0, 256, size=(n, PAGE_RECORDS, HEAD_DIM // 2), dtype=np.uint8)
+    recs[..., HEAD_DIM // 2:] = rng.integers(124, 129, size=(n, PAGE_RECORDS, HEAD_DIM // 32), dtype=np.uint8)
+    return dataclasses.replace(w, kv=kv, record_format="mxfp4", meta=dict(w.meta, record_format="mxfp4"))
 
 
 def _uniform(lo: int, hi: int):

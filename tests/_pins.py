@@ -736,4 +736,29 @@ def pin_fp4_logit_composes_rounding(o: O.Oracle):
         assert abs(got - want) <= 1e-12 * (1.0 + abs(want)), (t, got, want)
 
 
+def pin_fp4_paged_logits_match_records(o: O.Oracle):
+    """Over a paged MXFP4 cache (full history and resident pages) the oracle's logit at
+    every visible position is the per-record FP4 logit (pinned above) of the record
+    that the page table and the position name."""
+    for resident in (None, 2):
+        base = synth.make_workload("fp4p", num_q=3, history=[300, 130, 64], resident_pages=resident,
+                                   seed=47, threads=1)
+        w = synth.mxfp4_cache(base, seed=48)
+        P = O.Problem(w)
+        lg, valid, flags = o.logits(P)
+        assert flags == 0
+        checked = 0
+        for b in range(w.num_q):
+            req = b if w.q_req is None else int(w.q_req[b])
+            pos, col, _ = o.visible(P, b)
+            assert valid[b].sum() == len(col)
+            for n, c in zip(pos.tolist(), col.tolist()):
+                page = int(w.page_table[req, n // PAGE])
+                rec = w.kv[page, (n % PAGE) * 68:(n % PAGE + 1) * 68]
+                want = o.fp4_logit(rec, w.q[b], w.fused_w[b])
+                assert abs(lg[b, c] - want) <= 1e-12 * (1.0 + abs(want)), (b, n)
+                checked += 1
+        assert checked > 100
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -81,6 +81,9 @@ MUTATIONS = [
     ("fp4_query_unrounded", "for (int d = 0; d < OR_D; ++d) dot += k[d] * qr[d];",
      "for (int d = 0; d < OR_D; ++d) dot += k[d] * qf[d];"),
     ("fp4_relu_dropped", "const double relu = dot > 0.0 ? dot : 0.0;", "const double relu = dot;"),
+    ("fp4_paged_record_stride", "r * (P->format == 1 ? OR_FP4_REC_BYTES : OR_REC_BYTES)", "r * OR_REC_BYTES"),
+    ("fp4_paged_query_unrounded", "  if (P->format == 1) {\n    for (int h = 0; h < H; ++h) {",
+     "  if (P->format == 2) {\n    for (int h = 0; h < H; ++h) {"),
 ]
 
 

@@ -71,3 +71,16 @@ def test_fused_weight_recipe():
     w = synth.make_workload("w", num_q=64, history=[64] * 64, seed=4)
     x = w.fused_w.astype(np.float64) * np.sqrt(128.0) * np.sqrt(64.0)
     assert abs(x.std() - 1.0) < 0.03
+
+
+def test_mxfp4_cache_shape_and_determinism():
+    """68-byte records drawn directly (codes and block-scale bytes), same geometry
+    and rows as the workload it is made from, identical for the same seed."""
+    base = synth.make_workload("mx", num_q=2, history=[700, 130], seed=5, threads=1)
+    a, b = synth.mxfp4_cache(base, seed=9), synth.mxfp4_cache(base, seed=9)
+    assert a.record_format == "mxfp4" and a.kv.shape == (base.kv.shape[0], 64 * 68)
+    assert np.array_equal(a.kv, b.kv) and not np.array_equal(a.kv, synth.mxfp4_cache(base, seed=10).kv)
+    scales = a.kv.reshape(-1, 64, 68)[..., 64:]
+    assert scales.min() >= 124 and scales.max() <= 128
+    assert np.array_equal(a.page_table, base.page_table) and np.array_equal(a.q, base.q)
+    assert a.k_bytes() == int(a.visible_counts().sum()) * 68
