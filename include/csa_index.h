@@ -106,6 +106,11 @@ enum {
  *   resident mode  positions p*64 + r for each listed page p, r < 64, p*64 + r < L
  * The position n is the record's logical index in the request's history; it is what
  * top-k returns.
+ *
+ * Size limit: the CTAs split the rows' 256-record tiles (ceil(visible records / 256) per
+ * row, counted per row even when rows share a request), plus 4 per non-empty row when
+ * rows average at least 16 tiles, kept as 32-bit offsets: that total must stay below
+ * 2^31 (about 5 * 10^11 records scored per call).
  */
 typedef struct csa_index_args {
   const void* q;
@@ -216,7 +221,7 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
  * (row tile offsets and per-segment candidate slots) in a CSA_STATIC_SCRATCH_BYTES
  * array that every GPU loading the library holds until the process exits.
  *
- * Limit: the call needs 256-byte-rounded 4*(num_q+1) bytes plus
+ * Limit: the call needs 256-byte-rounded 4*(num_q+2) bytes plus
  * (num_q + number of SMs) * (16 + 8*min(1024, k + k/2) rounded up to 16) bytes of
  * that array (64 rows at k = 512 on a 152-SM GB300 use about 1.3 MB); larger requests return
  * CSA_ERR_WORKSPACE before anything is launched.
