@@ -271,7 +271,8 @@ enum { CSA_ENSEMBLE_MAX = 0, CSA_ENSEMBLE_MEAN = 1 };
  * Errors: as csa_index_score for each layer, plus CSA_ERR_INVALID_ARG for n_layers outside
  * [1, 8], an unknown ensemble, a NaN threshold, negative sink or recent, strides too small,
  * layers that disagree on num_q, num_req or pt_stride, or a resident list given; and
- * CSA_ERR_WORKSPACE when ws is smaller than csa_recall_workspace_bytes.
+ * CSA_ERR_WORKSPACE when ws is smaller than csa_recall_workspace_bytes; CSA_ERR_UNSUPPORTED
+ * for pt_stride above 65535 * 64 pages.
  */
 typedef struct csa_recall_args {
   const csa_index_args* layers;

@@ -152,6 +152,7 @@ extern "C" csa_status csa_recall_level1(const csa_recall_args* a, void* ws, size
   }
   const int64_t num_q = L0.num_q;
   if (num_q < 0 || L0.pt_stride < 1) return CSA_ERR_INVALID_ARG;
+  if ((L0.pt_stride + kWinPages - 1) / kWinPages > 65535) return CSA_ERR_UNSUPPORTED;  // grid y of keep_kernel
   if (num_q == 0) return CSA_OK;
   if (!a->keep || !a->pages || !a->n_pages) return CSA_ERR_INVALID_ARG;
   if (a->keep_stride < static_cast<int64_t>(kPage) * L0.pt_stride || a->pages_stride < L0.pt_stride)

@@ -217,6 +217,9 @@ def test_recall_rejects_bad_args(lib):
     assert call() == 1
     arr[1].pt_stride = 4
     assert call(layers=0) == 1
+    arr[0].pt_stride = arr[1].pt_stride = 65535 * 64 + 1  # more page windows than a grid dimension holds
+    assert call(pages_stride=65535 * 64 + 1, keep_stride=64 * (65535 * 64 + 1)) == 2
+    arr[0].pt_stride = arr[1].pt_stride = 4
     need = lib.csa_recall_workspace_bytes(ctypes.byref(native.RecallArgs(**base)))
     assert need > 0
     assert lib.csa_recall_level1(ctypes.byref(native.RecallArgs(**base)), ctypes.c_void_p(0x90000), need - 1,
