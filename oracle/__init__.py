@@ -125,6 +125,8 @@ def _bind(path: str):
     lib.oracle_fp4_decode.restype = None
     lib.oracle_fp4_logit.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
     lib.oracle_fp4_logit.restype = ctypes.c_double
+    lib.oracle_fp4_write_keys.argtypes = lib.oracle_write_keys.argtypes
+    lib.oracle_fp4_write_keys.restype = ctypes.c_int32
     return lib
 
 
@@ -255,6 +257,9 @@ class Oracle:
     def fp4_logit(self, rec, q_bits, w):
         return _fp4_logit(self.lib, rec, q_bits, w)
 
+    def fp4_write_keys(self, keys, req, pos, kv, page_table) -> int:
+        return _write_keys(self.lib, keys, req, pos, kv, page_table, fp4=True)
+
 
 def load_build(path: str) -> Oracle:
     """An Oracle bound to another build of csa_oracle.c (used by mutation tests)."""
@@ -366,16 +371,18 @@ def _quantise_row(lib, x):
     return rec, int(flags)
 
 
-def _write_keys(lib, keys, req, pos, kv, page_table) -> int:
+def _write_keys(lib, keys, req, pos, kv, page_table, fp4: bool = False) -> int:
     """Writes key rows into `kv` ([num_pages, page_stride] uint8, C-contiguous) in
-    place; returns the OR of the flag bits."""
+    place as e4m3 (132-byte) or, with fp4, MXFP4 (68-byte) records; returns the OR
+    of the flag bits."""
     k = np.ascontiguousarray(keys, dtype=np.float32)
     assert k.ndim == 2 and k.shape[1] == 128
     assert kv.dtype == np.uint8 and kv.flags["C_CONTIGUOUS"]
     p = np.ascontiguousarray(pos, dtype=np.int32)
     r = None if req is None else np.ascontiguousarray(req, dtype=np.int32)
     pt = np.ascontiguousarray(page_table, dtype=np.int32)
-    return int(lib.oracle_write_keys(k.ctypes.data, int(k.shape[0]), _ptr(r), p.ctypes.data, kv.ctypes.data,
+    fn = lib.oracle_fp4_write_keys if fp4 else lib.oracle_write_keys
+    return int(fn(k.ctypes.data, int(k.shape[0]), _ptr(r), p.ctypes.data, kv.ctypes.data,
                                      int(kv.shape[0]), int(kv.shape[1]), pt.ctypes.data, int(pt.shape[0]),
                                      int(pt.shape[1])))
 
@@ -490,3 +497,7 @@ def fp4_decode(rec):
 
 def fp4_logit(rec, q_bits, w):
     return _fp4_logit(_load(), rec, q_bits, w)
+
+
+def fp4_write_keys(keys, req, pos, kv, page_table) -> int:
+    return _write_keys(_load(), keys, req, pos, kv, page_table, fp4=True)

@@ -667,3 +667,38 @@ double oracle_fp4_logit(const uint8_t* rec, const uint16_t* q, const float* w, i
   }
   return logit;
 }
+
+/* Key rows written into a paged MXFP4 cache: the 68-byte record of row i goes to
+ * page_table[req][pos / 64], row pos % 64. The same checks as oracle_write_keys,
+ * in the same order (request, position, page, a non-finite value): a failing row
+ * is skipped and its flag bit set. */
+int32_t oracle_fp4_write_keys(const float* keys, int64_t n, const int32_t* req, const int32_t* pos, uint8_t* kv,
+                              int64_t num_pages, int64_t page_stride, const int32_t* page_table, int32_t num_req,
+                              int32_t pt_stride) {
+  int32_t flags = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t r = req ? req[i] : i;
+    if (r < 0 || r >= num_req) {
+      flags |= OR_FLAG_BAD_REQUEST;
+      continue;
+    }
+    const int64_t p = pos[i];
+    if (p < 0 || p >= (int64_t)OR_PAGE * pt_stride) {
+      flags |= OR_FLAG_LEN_OOB;
+      continue;
+    }
+    const int64_t phys = page_table[r * pt_stride + p / OR_PAGE];
+    if (phys < 0 || phys >= num_pages) {
+      flags |= OR_FLAG_PAGE_OOB;
+      continue;
+    }
+    int finite = 1;
+    for (int d = 0; d < OR_D; ++d) finite &= isfinite(keys[i * OR_D + d]) ? 1 : 0;
+    if (!finite) {
+      flags |= OR_FLAG_RANGE;
+      continue;
+    }
+    oracle_fp4_record(keys + i * OR_D, kv + phys * page_stride + (p % OR_PAGE) * OR_FP4_REC_BYTES);
+  }
+  return flags;
+}

@@ -761,4 +761,35 @@ def pin_fp4_paged_logits_match_records(o: O.Oracle):
         assert checked > 100
 
 
+def pin_fp4_writer(o: O.Oracle):
+    """The FP4 writer puts each valid row's record (oracle's fp4_record, pinned above)
+    at page_table[req][pos / 64], row pos % 64, touches nothing else, and skips and
+    flags a bad request, position, page or a non-finite value, in that order; the
+    paged oracle then reads the rows back as its keys."""
+    rng = np.random.default_rng(49)
+    num_req, pts, num_pages = 3, 2, 8
+    pt = rng.permutation(num_pages)[: num_req * pts].reshape(num_req, pts).astype(np.int32)
+    kv = np.full((num_pages, 64 * 68), 0xA5, dtype=np.uint8)
+    x = (rng.standard_normal((10, D)) * 10.0 ** rng.uniform(-3, 3, (10, 1))).astype(np.float32)
+    req = np.array([0, 1, 2, 0, 3, -1, 1, 2, 0, 1], np.int32)
+    pos = np.array([0, 70, 127, 5, 1, 2, 128, 64, 9, 30], np.int32)
+    x[8, 3] = np.nan
+    pt_bad = pt.copy()
+    pt_bad[2, 1] = num_pages + 1                       # row 7 (request 2, position 64) lands on a bad page
+    want = kv.copy()
+    for i in range(10):
+        if req[i] in (0, 1, 2) and 0 <= pos[i] < 128 and not (req[i] == 2 and pos[i] >= 64) and i != 8:
+            page = int(pt_bad[req[i], pos[i] // 64])
+            want[page, (pos[i] % 64) * 68:(pos[i] % 64 + 1) * 68] = o.fp4_record(x[i])
+    got = kv.copy()
+    flags = o.fp4_write_keys(x, req, pos, got, pt_bad)
+    assert flags == O.BAD_REQUEST | O.LEN_OOB | O.PAGE_OOB | O.RANGE, flags
+    assert np.array_equal(got, want)
+    # written rows read back through the paged oracle: record i is row pos % 64 of its page
+    for i in (0, 1, 3, 9):
+        page = int(pt[req[i], pos[i] // 64])
+        assert np.array_equal(o.fp4_decode(got[page, (pos[i] % 64) * 68:(pos[i] % 64 + 1) * 68]),
+                              o.fp4_decode(o.fp4_record(x[i])))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

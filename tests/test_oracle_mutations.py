@@ -84,6 +84,10 @@ MUTATIONS = [
     ("fp4_paged_record_stride", "r * (P->format == 1 ? OR_FP4_REC_BYTES : OR_REC_BYTES)", "r * OR_REC_BYTES"),
     ("fp4_paged_query_unrounded", "  if (P->format == 1) {\n    for (int h = 0; h < H; ++h) {",
      "  if (P->format == 2) {\n    for (int h = 0; h < H; ++h) {"),
+    ("fp4_writer_row_stride", "kv + phys * page_stride + (p % OR_PAGE) * OR_FP4_REC_BYTES);",
+     "kv + phys * page_stride + (p % OR_PAGE) * OR_REC_BYTES);"),
+    ("fp4_writer_nonfinite_kept", "    if (!finite) {\n      flags |= OR_FLAG_RANGE;\n      continue;\n    }\n    oracle_fp4_record(",
+     "    if (!finite) {\n      flags |= OR_FLAG_RANGE;\n    }\n    oracle_fp4_record("),
 ]
 
 
