@@ -49,7 +49,10 @@
 extern "C" {
 #endif
 
-#define CSA_ABI_VERSION 1
+/* Raised whenever an entry point, a struct layout or the meaning of an argument changes.
+ * 2: csa_index_logits, csa_index_write_keys and the Level-1 recall entry points; 128 heads
+ *    in the score and logit modes; a larger fused-path workspace (num_q + 2 row offsets). */
+#define CSA_ABI_VERSION 2
 
 #define CSA_HEAD_DIM 128        /* D: e4m3 bytes per record                         */
 #define CSA_NUM_HEADS 64        /* H of the Level-2 indexer                         */

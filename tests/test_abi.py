@@ -53,7 +53,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 
 def test_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 1
+    assert lib.csa_index_abi_version() == 2
     for s in range(6):
         assert native.status_str(s)
     assert native.status_str(99) == "unknown status"
