@@ -18,7 +18,7 @@
  *   BatchGen #153 commit log: relu is applied before the head-weighted sum;
  *     lengths count compressed records.
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - e4m3 is the OCP "fn" variant (bias 7, no infinities, S.1111.111 = NaN).
  *   - The trailing scale is little-endian IEEE binary32.
  *   - All arithmetic is fp64 (the pages' `.float()` dequant rounds k to fp32,
@@ -566,7 +566,7 @@ int32_t oracle_recall(const oracle_problem* layers, int32_t n_layers, int32_t en
  * page: the published model FP4-rounds the index query and key alike (e2m1,
  * "MXFP4", cvt.e2m1x2) before the index score. The pages name the element type
  * and MXFP4 but print neither the block size nor a record layout. Readings
- * (also listed in the design doc), following the OCP MX format for MXFP4:
+ * follow the OCP MX format for MXFP4:
  *   - blocks of 32 consecutive elements along head_dim share one UE8M0 scale
  *     X = 2^(floor(log2(amax)) - 2), 2 being the largest e2m1 exponent; the
  *     exponent is clamped to [-127, 127]; a block of zeros takes X = 2^-127;

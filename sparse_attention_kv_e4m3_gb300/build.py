@@ -11,7 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libcsa_index.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("csa_index.cu", "csa_writer.cu", "csa_recall.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("csa_ptx.cuh", "csa_select.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("csa_ptx.cuh", "csa_select.cuh", "csa_score64.cuh",
+                                                  "csa_internal.h")] + [
     os.path.join(INCLUDE, "csa_index.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -201,24 +201,27 @@ __device__ __forceinline__ int32_t resident_count(const Params& P, int32_t req, 
   return n;
 }
 
-// Tiles (kTilePages page slots each) that row b covers.
+// Tiles (TP page slots each) that row b covers.
+template <int TP = kTilePages>
 __device__ __forceinline__ int64_t query_tiles(const Params& P, int32_t b, int32_t* flags) {
   const int32_t req = row_request(P, b);
   if (req < 0) {
     *flags |= CSA_DEV_BAD_REQUEST;
     return 0;
   }
-  if (P.resident) return (resident_count(P, req, flags) + kTilePages - 1) / kTilePages;
-  return (row_length(P, b, flags) + kTile - 1) / kTile;
+  if (P.resident) return (resident_count(P, req, flags) + TP - 1) / TP;
+  return (row_length(P, b, flags) + kPage * TP - 1) / (kPage * TP);
 }
 
+template <int TP = kTilePages>
 __device__ __forceinline__ int64_t query_tiles(const Params& P, int32_t b) {
   int32_t f = 0;
-  return query_tiles(P, b, &f);
+  return query_tiles<TP>(P, b, &f);
 }
 
+template <int TP = kTilePages>
 __device__ __forceinline__ int32_t next_nonempty(const Params& P, int32_t b) {
-  while (b < P.num_q && query_tiles(P, b) == 0) ++b;
+  while (b < P.num_q && query_tiles<TP>(P, b) == 0) ++b;
   return b;
 }
 
@@ -232,15 +235,16 @@ __host__ __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t total, int
   return c < grid - 1 ? c : grid - 1;
 }
 
-// Visible rows, logical page and physical page of page slot `j` (0..3) of tile
-// `lt` of row b. nrows = 0 marks a slot with nothing to score.
+// Visible rows, logical page and physical page of page slot `j` (0..TP-1) of
+// tile `lt` of row b. nrows = 0 marks a slot with nothing to score.
+template <int TP = kTilePages>
 __device__ PageInfo page_of(const Params& P, int32_t b, int64_t lt, int j, int32_t* flags) {
   PageInfo e{0, 0, 0, 0};
   const int32_t req = row_request(P, b);
   if (req < 0) return e;
   const int64_t L = row_length(P, b, flags);
   const int64_t npages = (L + kPage - 1) / kPage;
-  const int64_t slot = kTilePages * lt + j;
+  const int64_t slot = static_cast<int64_t>(TP) * lt + j;
   int64_t p;
   if (P.resident) {
     if (slot >= resident_count(P, req, flags)) return e;
@@ -278,8 +282,10 @@ __device__ PageInfo page_of(const Params& P, int32_t b, int64_t lt, int j, int32
 // tiles of time, and without the charge the CTAs that cross a row boundary
 // finished last. Batches of short rows (chunked prefill) keep the plain split:
 // there the charge made a few CTAs several times slower, for reasons not yet
-// understood.
-constexpr int64_t kSegTiles = 4, kLongRowTiles = 16;
+// understood. Both figures are in records, so that they mean the same for
+// every tile size: a row start costs 1024 records, and rows count as long from
+// 4096 records on average.
+constexpr int64_t kSegRecords = 1024, kLongRowRecords = 4096;
 
 struct Plan {
   int64_t total;   // virtual tiles of all rows
@@ -296,8 +302,9 @@ struct Plan {
 // sums of the virtual tiles (tile_off[0 .. num_q]) and the charge per row W
 // (tile_off[num_q + 1]): row b's tiles are virtual tiles tile_off[b] + W ..
 // tile_off[b + 1] - 1.
-template <int NT>
+template <int NT, int TP = kTilePages>
 __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32_t* tile_off) {
+  constexpr int64_t kSegTiles = kSegRecords / (kPage * TP), kLongRowTiles = kLongRowRecords / (kPage * TP);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
   int32_t flags = 0;
@@ -308,7 +315,7 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
   // pass 1: real tiles and non-empty rows, hence the charge per row and the virtual total
   int64_t part = 0;
   for (int32_t b = tid; b < P.num_q; b += NT) {
-    const int64_t t = query_tiles(P, b, &flags);
+    const int64_t t = query_tiles<TP>(P, b, &flags);
     part += t | (t > 0 ? int64_t{1} << kShift : 0);
   }
 #pragma unroll
@@ -339,7 +346,7 @@ __device__ void make_plan(const Params& P, Plan* plan, int64_t* warp_sums, int32
   int64_t running = 0;
   for (int32_t base = 0; base < P.num_q; base += NT) {
     const int32_t b = base + tid;
-    const int64_t tr = b < P.num_q ? query_tiles(P, b) : 0;
+    const int64_t tr = b < P.num_q ? query_tiles<TP>(P, b) : 0;
     const int64_t t = tr > 0 ? (tr + W) | (int64_t{1} << kShift) : 0;
     int64_t incl = t;
 #pragma unroll
@@ -453,36 +460,39 @@ __device__ __forceinline__ Smem<H>& smem_of(uint8_t* raw) {
 
 // ------------------------------------------------------------------ roles
 
-struct Cursor {
+template <int TP = kTilePages>
+struct CursorT {
   int32_t b;
   int64_t lt;
   int64_t tiles;
   __device__ void init(const Params& P, const Plan& pl) {
     b = pl.b0;
     lt = pl.lt0;
-    tiles = b < P.num_q ? query_tiles(P, b) : 0;
+    tiles = b < P.num_q ? query_tiles<TP>(P, b) : 0;
   }
   __device__ void advance(const Params& P) {
     if (++lt >= tiles) {
-      b = next_nonempty(P, b + 1);
+      b = next_nonempty<TP>(P, b + 1);
       lt = 0;
-      tiles = b < P.num_q ? query_tiles(P, b) : 0;
+      tiles = b < P.num_q ? query_tiles<TP>(P, b) : 0;
     }
   }
 };
+using Cursor = CursorT<>;
 
 // Broadcast of lane 0's value to the warp.
 __device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0; }
 
 
-template <int H>
-__device__ void role_walker(const Params& P, Smem<H>& S) {
-  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
-  (void)kStages;
-  (void)kDStages;
+// Page walker: fills the ring with the PageInfo of the CTA's pages, 32 at a
+// time (TP page slots per tile; 32 / TP tiles per ring slot). SM is the
+// kernel's shared-memory struct (ring, rfull, rempty, plan, abort_flag, status).
+template <int TP, class SM>
+__device__ void walk_pages(const Params& P, SM& S) {
+  static_assert(32 % TP == 0, "a ring slot holds whole tiles");
   const int lane = threadIdx.x & 31;
-  const int64_t npg = kTilePages * S.plan.ntiles;
-  Cursor cur;
+  const int64_t npg = static_cast<int64_t>(TP) * S.plan.ntiles;
+  CursorT<TP> cur;
   cur.init(P, S.plan);
   int32_t flags = 0;
   for (int64_t pg = 0; pg < npg; pg += 32) {
@@ -492,25 +502,30 @@ __device__ void role_walker(const Params& P, Smem<H>& S) {
     if (lane == 0) ok = mbar_wait(smem_u32(&S.rempty[slot]), static_cast<uint32_t>(((batch / kRing) & 1) ^ 1),
                                   &S.abort_flag);
     if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-    // lane j handles page pg + j: tile offset j / 4, slot j % 4
+    // lane j handles page pg + j: tile offset j / TP, slot j % TP
     int32_t bb = cur.b;
-    int64_t ll = cur.lt + lane / kTilePages, tb = cur.tiles;
+    int64_t ll = cur.lt + lane / TP, tb = cur.tiles;
     while (bb < P.num_q && ll >= tb) {
       ll -= tb;
-      bb = next_nonempty(P, bb + 1);
-      tb = bb < P.num_q ? query_tiles(P, bb) : 0;
+      bb = next_nonempty<TP>(P, bb + 1);
+      tb = bb < P.num_q ? query_tiles<TP>(P, bb) : 0;
     }
     PageInfo e{0, -1, 0, 0};
-    if (pg + lane < npg && bb < P.num_q) e = page_of(P, bb, ll, lane % kTilePages, &flags);
+    if (pg + lane < npg && bb < P.num_q) e = page_of<TP>(P, bb, ll, lane % TP, &flags);
     S.ring[slot * 32 + lane] = e;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.rfull[slot]));
     // the cursor moves on by 32 pages
-    for (int t = 0; t < 32 / kTilePages; ++t) cur.advance(P);
+    for (int t = 0; t < 32 / TP; ++t) cur.advance(P);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
   if (lane == 0 && flags) atomicOr(&S.status, flags);
+}
+
+template <int H>
+__device__ void role_walker(const Params& P, Smem<H>& S) {
+  walk_pages<kTilePages>(P, S);
 }
 
 // Page copies are issued by kIssueLanes lanes in lockstep, one page each: the
@@ -678,8 +693,8 @@ __device__ __forceinline__ uint32_t qbuf_offset(int h, int chunk) {
 // loads are issued before the previous batch is processed: the first query of
 // a CTA is prepared while every CTA's first page copies load HBM, and a loop
 // that waits for memory once per head or per batch took about 11 us there.
-template <int H>
-__device__ void prep_query(const Params& P, Smem<H>& S, int32_t b, int qs, int32_t* flags) {
+template <int H, class SM>
+__device__ void prep_query(const Params& P, SM& S, int32_t b, int qs, int32_t* flags) {
   const int lane = threadIdx.x & 31;
   const uint16_t* qrow = P.q + static_cast<int64_t>(b) * H * kD;
   const float* wrow = P.w + static_cast<int64_t>(b) * H;
@@ -751,8 +766,8 @@ __device__ void prep_query(const Params& P, Smem<H>& S, int32_t b, int qs, int32
 // elements 16p .. 16p+15 of head h = t / 8 (p = t % 8), so that the row's loads
 // are all issued at once. Same arithmetic and layout as prep_query.
 static_assert(kThreads == 64 * (kD / 16), "64 heads per pass, one thread per 16 elements");
-template <int H>
-__device__ void prep_first_query(const Params& P, Smem<H>& S, int32_t b, int32_t* flags) {
+template <int H, class SM>
+__device__ void prep_first_query(const Params& P, SM& S, int32_t b, int32_t* flags) {
   const int tid = threadIdx.x, p = tid & 7;
 #pragma unroll
   for (int pass = 0; pass < H / 64; ++pass) {
@@ -792,32 +807,36 @@ __device__ void prep_first_query(const Params& P, Smem<H>& S, int32_t b, int32_t
 }
 
 // Prepares the queries of the CTA's later segments (the first one is prepared
-// in the prologue), each as soon as its slot is free.
-template <int H>
-__device__ void role_qprep(const Params& P, Smem<H>& S) {
-  constexpr int kStages = Smem<H>::kStages, kDStages = Smem<H>::kDStages;
-  (void)kStages;
-  (void)kDStages;
+// in the prologue), each as soon as its slot is free. TP: pages per tile of the
+// calling kernel; SM: its shared-memory struct (qbuf, wbuf, qfull, qempty, plan,
+// abort_flag, status).
+template <int H, int TP, class SM>
+__device__ void prep_segments(const Params& P, SM& S) {
   const int lane = threadIdx.x & 31;
   int32_t flags = 0;
-  int64_t done = query_tiles(P, S.plan.b0) - S.plan.lt0;
-  int32_t b = next_nonempty(P, S.plan.b0 + 1);
+  int64_t done = query_tiles<TP>(P, S.plan.b0) - S.plan.lt0;
+  int32_t b = next_nonempty<TP>(P, S.plan.b0 + 1);
   for (int seg = 1; done < S.plan.ntiles; ++seg) {
     const int qs = seg & 1;
     int ok = 1;
     if (lane == 0)
       ok = mbar_wait(smem_u32(&S.qempty[qs]), static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), &S.abort_flag);
     if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-    prep_query(P, S, b, qs, &flags);
+    prep_query<H>(P, S, b, qs, &flags);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&S.qfull[qs]));
-    done += query_tiles(P, b);
-    b = next_nonempty(P, b + 1);
+    done += query_tiles<TP>(P, b);
+    b = next_nonempty<TP>(P, b + 1);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
   if (lane == 0 && flags) atomicOr(&S.status, flags);
+}
+
+template <int H>
+__device__ void role_qprep(const Params& P, Smem<H>& S) {
+  prep_segments<H, kTilePages>(P, S);
 }
 
 // One warp of a worker group: TMEM lane quarter q of every tile the group owns
@@ -1185,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
   }
   {
     int32_t qflags = 0;
-    prep_first_query(P, S, S.plan.b0, &qflags);
+    prep_first_query<H>(P, S, S.plan.b0, &qflags);
     fence_proxy_async_smem();  // the MMA reads the query through the async proxy
     if (qflags) atomicOr(&S.status, qflags);
   }
@@ -1219,6 +1238,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const Params P) {
     if (st) atomicOr(P.dev_status, st);
   }
 }
+
+}  // namespace csa
+
+#include "csa_score64.cuh"
+
+namespace csa {
 
 // ------------------------------------------------------------------ merge
 
@@ -1496,10 +1521,10 @@ csa_status device_setup(int* sms) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return CSA_ERR_CUDA;
     if (n * kTopkCtasPerSm > CSA_MAX_CTAS) return CSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(score_kernel<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes<64>)) != cudaSuccess ||
-        cudaFuncSetAttribute(score_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes<64>)) != cudaSuccess ||
+    if (cudaFuncSetAttribute(w64::score_kernel_w64<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(w64::score_kernel_w64<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(score_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes<128>)) != cudaSuccess ||
         cudaFuncSetAttribute(merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1545,13 +1570,23 @@ csa_status launch_status() { return cudaGetLastError() == cudaSuccess ? CSA_OK :
 
 }  // namespace
 
-// Score or logit mode (P.raw_logits) of the scoring kernel for 64 or 128 heads.
-void launch_score(const Params& P, int32_t num_heads, int sms, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (num_heads == 2 * kH)
-    score_kernel<false, 128><<<sms, kThreads, kSmemBytes<128>, s>>>(P);
+// The 64-head scorer in score / logit mode or top-k mode.
+csa_status launch_w64(const Params& P, bool topk, int sms, cudaStream_t s) {
+  if (topk)
+    w64::score_kernel_w64<true><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
   else
-    score_kernel<false, 64><<<sms, kThreads, kSmemBytes<64>, s>>>(P);
+    w64::score_kernel_w64<false><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
+  return launch_status();
+}
+
+// Score or logit mode (P.raw_logits) of the scoring kernel for 64 or 128 heads.
+csa_status launch_score(const csa_index_args* a, const Params& P, int sms, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->num_heads == 2 * kH) {
+    score_kernel<false, 128><<<sms, kThreads, kSmemBytes<128>, s>>>(P);
+    return launch_status();
+  }
+  return launch_w64(P, false, sms, s);
 }
 
 extern "C" {
@@ -1589,8 +1624,7 @@ csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t sc
   P.scores = scores;
   P.score_stride = score_stride;
   P.grid = sms;
-  launch_score(P, args->num_heads, sms, stream);
-  return launch_status();
+  return launch_score(args, P, sms, stream);
 }
 
 csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t stride, void* stream) {
@@ -1607,8 +1641,7 @@ csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t s
   P.score_stride = stride;
   P.grid = sms;
   P.raw_logits = 1;
-  launch_score(P, args->num_heads, sms, stream);
-  return launch_status();
+  return launch_score(args, P, sms, stream);
 }
 
 }  // extern "C"
@@ -1618,6 +1651,7 @@ csa_status csa_score_fold(const csa_index_args* args, float* acc, int64_t stride
   if (st != CSA_OK) return st;
   if (args->num_q == 0) return CSA_OK;
   if (!acc || args->resident || (fold != CSA_FOLD_MAX && fold != CSA_FOLD_ADD)) return CSA_ERR_INVALID_ARG;
+  if (args->num_heads != 2 * kH) return CSA_ERR_UNSUPPORTED;  // the fold mode is the 128-head scorer's
   if (!aligned(acc, 4)) return CSA_ERR_ALIGNMENT;
   if (stride < min_score_stride(args)) return CSA_ERR_INVALID_ARG;
   int sms = 0;
@@ -1627,8 +1661,7 @@ csa_status csa_score_fold(const csa_index_args* args, float* acc, int64_t stride
   P.score_stride = stride;
   P.grid = sms;
   P.fold = fold;
-  launch_score(P, args->num_heads, sms, stream);
-  return launch_status();
+  return launch_score(args, P, sms, stream);
 }
 
 extern "C" {
@@ -1657,8 +1690,7 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
   P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
   P.grid = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  score_kernel<true, 64><<<sms, kThreads, kSmemBytes<64>, s>>>(P);
-  if ((st = launch_status()) != CSA_OK) return st;
+  if ((st = launch_w64(P, true, sms, s)) != CSA_OK) return st;
   if (event && cudaEventRecord(static_cast<cudaEvent_t>(event), s) != cudaSuccess) return CSA_ERR_CUDA;
   merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
   return launch_status();
@@ -1749,8 +1781,7 @@ extern "C" csa_status csa_index_score_topk_fused_static(const csa_index_args* ar
   P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
   P.grid = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  score_kernel<true, 64><<<sms, kThreads, kSmemBytes<64>, s>>>(P);
-  if ((st = launch_status()) != CSA_OK) return st;
+  if ((st = launch_w64(P, true, sms, s)) != CSA_OK) return st;
   merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
   return launch_status();
 }

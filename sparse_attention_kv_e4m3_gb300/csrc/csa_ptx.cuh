@@ -1,6 +1,7 @@
 // csa_ptx.cuh — inline-PTX building blocks for sm_103a: mbarriers with bounded
-// waits, 1-D bulk copies (global -> shared), and the tcgen05 tensor-core ops
-// (TMEM alloc, MMA with A in TMEM, commit, TMEM loads/stores, fences).
+// waits, 1-D bulk copies and tiled tensor copies (global -> shared), and the
+// tcgen05 tensor-core ops (TMEM alloc, MMA with A in TMEM or shared memory,
+// commit, TMEM loads/stores, fences).
 #pragma once
 
 #include <cstdint>
@@ -164,6 +165,22 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// Tiled 3-D tensor copy global -> this CTA's shared memory through the tensor
+// map at `tmap` (a kernel parameter), box origin (x, y, z), completing as the
+// box's bytes on `bar`. x times the element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -211,6 +228,34 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// K-major operand in the 32-byte swizzle layout: rows of 32 bytes (one MMA's
+// K = 32 of 8-bit elements), 8-row atoms of 256 bytes stacked along M (stride
+// 256 B), swizzle mode 6 (32 B).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(6u) << 61;
+  return d;
+}
+
+// MN-major operand in the 128-byte swizzle layout: a row holds 128 consecutive
+// N elements (8-bit) at one K index, 8 consecutive K rows form a 1024-byte
+// atom, and atoms follow each other along K (stride-dimension offset 1024 B).
+// The leading-dimension offset (next 128-element group along N) is given for
+// completeness; operands here are exactly 128 wide.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of a dense kind::f8f6f4 MMA with e4m3 A and B, both
 // K-major, fp32 accumulator, shape M x N: accumulator format in bits 4-5
 // (1 = f32), A / B formats in bits 7-9 / 10-12 (0 = e4m3), N >> 3 in bits
@@ -227,6 +272,20 @@ __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// B operand MN-major (bit 16 of the instruction descriptor: transpose B).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one CTA, kind::f8f6f4 (K = 32 per call).
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -250,6 +309,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
       "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+// 32 lanes x 32 bits, 8 consecutive columns: thread t writes lane (base + t).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {

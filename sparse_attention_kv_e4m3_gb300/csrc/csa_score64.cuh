@@ -1,0 +1,604 @@
+// csa_score64.cuh — the 64-head scoring kernel (the indexer's hot path).
+//
+// Included by csa_index.cu after the shared definitions (Params, PageInfo, the
+// plan, the page walker, the query preparation, the selection helpers).
+//
+// Data path. Whole 8448-byte pages are streamed into a ring of shared-memory
+// slots with 1-D bulk copies (one copy-engine instruction per page: measured on
+// this GPU, tiled tensor copies of the page's rows cost about 140 cycles per
+// box and 7.6 per 128-byte row, which caps them below the HBM rate). A record
+// is 132 bytes, so record rows are not 16-byte aligned; four records are
+// (528 = 33 x 16). The records of a page are therefore taken in "classes":
+// class r (r = 0..3) is record r of each of the page's 16 four-record groups,
+// and record r of group g starts 4r bytes past the 16-byte-aligned offset
+// 528g + 128r. A worker thread loads the nine aligned 16-byte chunks from there
+// (conflict-free across a warp) and passes words r .. r + 31 — exactly the
+// record's 128 key bytes — to its TMEM lane; word r + 32 is the record's
+// fp32 scale. Every lane of a warp works on the same class, so the word
+// selection is a warp-uniform choice between four register assignments.
+//
+// A class sub-tile is record r of the 128 groups of one tile (8 pages = 512
+// records): TMEM lane m holds group m % 16 of page m / 16. It is scored by
+// M=128, N=64, K=32 e4m3 MMAs with the key bytes in TMEM (A) and the query in
+// shared memory (B, K-major, one buffer per term): the query's e4m3 hi term
+// over K = 0..127 (four MMAs), then its lo term into the same accumulator (four
+// more), so each head's column holds k . (q * 2^e_h) itself. A half-tile is two
+// class sub-tiles (classes 2g and 2g + 1 of a tile) and belongs to worker group
+// g; a worker lane then carries two records per iteration, which amortises the
+// iteration's fixed barrier and hand-off latencies. The MMA warp issues a
+// half-tile's 16 MMAs back to back from precomputed operands: measured here, a
+// thread issues at most one tcgen05.mma every ~50 cycles in a tight loop (and
+// two issuing warps reach the tensor pipe's ~32 cycles per N=64 MMA), while a
+// loop that rebuilds descriptors and branches per MMA takes ~95-106.
+//
+// Warp roles (512 threads):
+//   0      issuer: 8 lanes in lockstep, one 1-D bulk copy per page into a ring of
+//          kPages slots
+//   1      MMA (one thread); allocates the 512 TMEM columns
+//   2      page walker (shared with the other scorer)
+//   3      query preparation for the CTA's later segments (the first is split
+//          by the whole CTA in the prologue); two query slots
+//   4-11   workers, two groups of four (one warp per TMEM lane quarter): group
+//          g owns classes 2g and 2g + 1 of every tile. For each tile: wait for
+//          the MMAs of its half-tile, stage the next tile's half-tile into the
+//          group's TMEM A stage (its MMAs then overlap), then the epilogue of
+//          both records.
+//   12-15  selector (top-k mode): one tile of keys (all four classes) per step
+//
+// TMEM: one 64-column A stage per worker group (columns 0 and 64: two class
+// sub-tiles of 32 columns) and three 128-column accumulator stages (columns
+// 128, 256, 384: two class sub-tiles of 64 columns).
+#pragma once
+
+namespace csa {
+namespace w64 {
+
+constexpr int kH = 64;
+constexpr int kTP = 8;                               // pages per tile
+constexpr int kTileRecs = kTP * kPage;               // 512
+constexpr int kGroupBytes = 4 * kRec;                // 528
+constexpr int kGroupsPerPage = kPage / 4;            // 16
+constexpr int kRows = kTP * kGroupsPerPage;          // 128 rows per class sub-tile (MMA M)
+constexpr int kPages = 17;                           // page ring slots
+constexpr int kDStages = 3;                          // accumulator stages
+constexpr int kKeyRing = 4;                          // tiles of keys, workers -> selector
+constexpr int kCapW = 2048;                          // candidate buffer of one segment
+constexpr int kThreads = 512;
+constexpr int kWarpIssuer = 0, kWarpMma = 1, kWarpWalker = 2, kWarpQprep = 3, kWarpWorker = 4, kWarpSelect = 12;
+constexpr int kWorkerWarps = 8;
+constexpr int kBarSelect = 1;
+constexpr int kQEmptyCount = 1 + kWorkerWarps;       // MMA commit + every worker warp
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, kH);
+
+__host__ __device__ constexpr uint32_t a_col(int g) { return 64u * static_cast<uint32_t>(g); }
+__host__ __device__ constexpr uint32_t d_col(int s) { return 128u + 128u * static_cast<uint32_t>(s); }
+
+static_assert(kGroupBytes % 16 == 0 && kPageBytes % 16 == 0, "group offsets and pages are 16-byte aligned");
+static_assert(kH == 64, "one N = 64 B operand per query term");
+static_assert(kCapW >= CSA_MAX_K + kTileRecs, "a cut leaves room for one more tile of keys");
+static_assert(a_col(2) <= d_col(0) && d_col(kDStages) <= kTmemCols, "TMEM column map");
+static_assert(32 % kTP == 0 && kTP == 8, "a walker ring slot holds four tiles; the issuer uses 8 lanes");
+static_assert(kThreads == 64 * (kD / 16), "the prologue splits the first query with one thread per 16 elements");
+
+struct __align__(1024) Smem {
+  uint8_t qbuf[2][2][kH * kD];                // [slot][hi/lo] e4m3, K-major, 128-byte swizzle: N=64 operands
+  uint8_t pages[kPages][kPageBytes];
+  uint64_t cand[kCapW];
+  uint64_t scratch[CSA_MAX_K];
+  uint64_t keys[kKeyRing][kTileRecs];         // a tile's admissible keys: 32 per (class, worker warp)
+  alignas(16) uint32_t kcnt[kKeyRing][16];    // keys in region 4 * class + lane quarter
+  PageInfo ring[kRing * 32];
+  PageInfo info[kPages];
+  int64_t last_pg[kPages];                    // most recent page copied into each ring slot (-1: none)
+  alignas(16) float wbuf[2][kH];              // head weights x 2^-e_h, by query slot
+  uint64_t full[kPages], empty[kPages];
+  uint64_t afull[2];
+  uint64_t dfull[kDStages], dempty[kDStages];
+  uint64_t kfull[kKeyRing], kempty[kKeyRing];
+  uint64_t rfull[kRing], rempty[kRing];
+  uint64_t qfull[2], qempty[2];
+  uint64_t drain;
+  uint64_t filt;                              // (segment << 32) | value word of the selector's threshold
+  SelectShared sel;
+  Plan plan;
+  int64_t warp_sums[32];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t status;
+  int32_t go[2];
+};
+
+constexpr bool smem_layout_ok() {
+  return offsetof(Smem, qbuf) % 1024 == 0 && offsetof(Smem, pages) % 16 == 0 && offsetof(Smem, wbuf) % 16 == 0 &&
+         offsetof(Smem, full) % 8 == 0 && offsetof(Smem, filt) % 8 == 0;
+}
+static_assert(smem_layout_ok(), "swizzle atoms 1024-byte aligned, copies 16-byte, mbarriers 8-byte aligned");
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ Smem& smem_of(uint8_t* raw) {
+  return *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint32_t filter_word(const Smem& S, int seg) {
+  const uint64_t f = *reinterpret_cast<const volatile uint64_t*>(&S.filt);
+  return static_cast<uint32_t>(f >> 32) == static_cast<uint32_t>(seg) ? static_cast<uint32_t>(f) : 0u;
+}
+
+// Packed fp32 pairs (two IEEE binary32 operations per instruction, round to nearest).
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ------------------------------------------------------------------ issuer
+
+// Lanes 0..7 copy the 8 pages of each tile in lockstep, page j of tile t into
+// ring slot (8t + j) % kPages.
+__device__ void role_issuer(const Params& P, Smem& S) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nt = S.plan.ntiles;
+  const uint64_t policy = policy_evict_first();
+  for (int s = lane; s < kPages; s += 32) S.last_pg[s] = -1;
+  __syncwarp();
+  for (int64_t t = 0; t < nt; ++t) {
+    const int64_t batch = t >> 2;  // a walker ring slot holds 32 pages = 4 tiles
+    const int rs = static_cast<int>(batch % kRing);
+    const uint32_t rph = static_cast<uint32_t>((batch / kRing) & 1);
+    if ((t & 3) == 0) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(smem_u32(&S.rfull[rs]), rph, &S.abort_flag);
+      if (!warp_ok(ok)) break;
+    }
+    bool ok = true;
+    if (lane < kTP) {
+      mbar_wait_drain(smem_u32(&S.rfull[rs]), rph);  // complete: acquire the walker's entries
+      const PageInfo e = S.ring[rs * 32 + static_cast<int>(t & 3) * kTP + lane];
+      const int64_t pg = kTP * t + lane;
+      const int s = static_cast<int>(pg % kPages);
+      ok = mbar_wait(smem_u32(&S.empty[s]), static_cast<uint32_t>(((pg / kPages) & 1) ^ 1), &S.abort_flag);
+      if (ok) {
+        S.info[s] = e;
+        const uint32_t fb = smem_u32(&S.full[s]);
+        if (e.nrows > 0) {
+          mbar_arrive_expect_tx(fb, kPageBytes);
+          bulk_g2s_hint(smem_u32(S.pages[s]), P.kv + static_cast<int64_t>(e.phys) * P.page_stride, kPageBytes, fb,
+                        policy);
+        } else {
+          mbar_arrive(fb);
+        }
+        S.last_pg[s] = pg;
+      }
+    }
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    if (lane == 0 && ((t & 3) == 3 || t == nt - 1)) mbar_arrive(smem_u32(&S.rempty[rs]));
+  }
+  // Every copy issued must land before the CTA may exit: the most recent one of
+  // each ring slot (a slot's earlier pages were consumed before it was reused).
+  __syncwarp();
+  for (int s = lane; s < kPages; s += 32) {
+    const int64_t p = S.last_pg[s];
+    if (p >= 0) mbar_wait_drain(smem_u32(&S.full[s]), static_cast<uint32_t>((p / kPages) & 1));
+  }
+}
+
+// ------------------------------------------------------------------ MMA
+
+__device__ void role_mma(const Params& P, Smem& S) {
+  CursorT<kTP> cur;
+  cur.init(P, S.plan);
+  const uint32_t tmem = S.tmem_base;
+  int seg = 0;
+  bool ok = true;
+  uint64_t bdesc[2][4];  // B descriptors of the current query slot: [hi/lo][K step]
+  for (int64_t t = 0; ok && t < S.plan.ntiles; ++t) {
+    const bool seg_start = (t == 0) || (cur.lt == 0);
+    if (seg_start && t > 0) ++seg;
+    const int qs = seg & 1;
+    if (seg_start) {
+      if (!mbar_wait(smem_u32(&S.qfull[qs]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag)) break;
+#pragma unroll
+      for (int term = 0; term < 2; ++term)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) bdesc[term][kk] = sdesc_kmajor_sw128(smem_u32(S.qbuf[qs][term]) + 32 * kk);
+    }
+#pragma unroll 1
+    for (int g = 0; g < 2; ++g) {  // the two half-tiles of tile t
+      const uint32_t h = static_cast<uint32_t>(2 * t + g);  // half-tiles of a CTA stay far below 2^32
+      const int ds = static_cast<int>(h % kDStages);
+      ok = mbar_wait(smem_u32(&S.afull[g]), static_cast<uint32_t>(t & 1), &S.abort_flag) &&
+           mbar_wait(smem_u32(&S.dempty[ds]), ((h / kDStages) & 1) ^ 1, &S.abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem + d_col(ds), a = tmem + a_col(g);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int term = 0; term < 2; ++term)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_e4m3_ts(d + kH * c, a + 32 * c + 8 * kk, bdesc[term][kk], kIdesc, (term | kk) != 0);
+      mma_commit(smem_u32(&S.dfull[ds]));
+    }
+    if (!ok) break;
+    const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
+    if (seg_end) mma_commit(smem_u32(&S.qempty[qs]));
+    cur.advance(P);
+  }
+  mma_commit(smem_u32(&S.drain));
+  mbar_wait_drain(smem_u32(&S.drain), 0);
+}
+
+// ------------------------------------------------------------------ workers
+
+// Words R .. R + 31 of the 36 loaded (the record's key bytes) into v; word
+// R + 32 (its scale) into sc.
+template <int R>
+__device__ __forceinline__ void pick_record(const uint32_t (&w)[36], uint32_t (&v)[32], uint32_t& sc) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = w[R + j];
+  sc = w[R + 32];
+}
+
+// Loads the 36 words at src (9 aligned 16-byte chunks): a record of class R
+// and its scale are words R .. R + 32.
+__device__ __forceinline__ void load36(const uint8_t* src, uint32_t (&w)[36]) {
+#pragma unroll
+  for (int j = 0; j < 9; ++j) {
+    const uint4 c = *reinterpret_cast<const uint4*>(src + 16 * j);
+    w[4 * j] = c.x;
+    w[4 * j + 1] = c.y;
+    w[4 * j + 2] = c.z;
+    w[4 * j + 3] = c.w;
+  }
+}
+
+// Stages this lane's record of class r (run-time, warp-uniform) from the
+// 16-byte-aligned group row `row` into TMEM column address ta; returns the
+// record's scale bits. The class is deliberately a run-time value selected by a
+// switch: every variant of the kernel that ran cleanly staged records this way,
+// while two variants whose class was a compile-time constant at this point
+// raised "illegal instruction" on the GPU (cause not identified).
+__device__ __forceinline__ uint32_t stage_record(const uint8_t* row, int r, uint32_t ta) {
+  uint32_t w[36];
+  load36(row + 128 * r, w);
+  uint32_t v[32], scale;
+  switch (r) {  // warp-uniform: every lane stages the same class
+    case 0: pick_record<0>(w, v, scale); break;
+    case 1: pick_record<1>(w, v, scale); break;
+    case 2: pick_record<2>(w, v, scale); break;
+    default: pick_record<3>(w, v, scale); break;
+  }
+  tmem_st32(ta, v);
+  return scale;
+}
+
+// One warp of a worker group: group gi owns classes 2gi and 2gi + 1 of every tile.
+template <bool kTopk>
+__device__ void role_worker(const Params& P, Smem& S) {
+  const int e = (threadIdx.x >> 5) - kWarpWorker;  // 0..7
+  const int gi = e >> 2;                            // worker group
+  const int c0 = 2 * gi;                            // the group's first class
+  const int q = e & 3;                              // TMEM lane quarter (warp index % 4)
+  const int lane = threadIdx.x & 31;
+  const int m = 32 * q + lane;                      // row of a class sub-tile: page m / 16, group m % 16
+  const int pg_in_tile = m >> 4, grp = m & 15;
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tmem = S.tmem_base;
+  const int64_t nt = S.plan.ntiles;
+
+  // Stages the group's half-tile of tile t into its A stage: this lane's two
+  // records (group grp of page pg_in_tile, records c0 and c0 + 1 of the group).
+  // Returns false on abort; sets each record's scale bits (NaN when the record
+  // is not visible) and position.
+  auto stage = [&](int64_t t, uint32_t (&sc)[2], uint32_t (&pos)[2]) -> bool {
+    const int64_t pg = kTP * t + pg_in_tile;
+    const int s = static_cast<int>(pg % kPages);
+    const bool ok = mbar_wait(smem_u32(&S.full[s]), static_cast<uint32_t>((pg / kPages) & 1), &S.abort_flag);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    const PageInfo pi = S.info[s];
+    const uint8_t* row = S.pages[s] + grp * kGroupBytes;
+    const uint32_t ta = tmem + a_col(gi) + lane_off;
+    sc[0] = stage_record(row, c0, ta);
+    sc[1] = stage_record(row, c0 + 1, ta + 32);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.afull[gi]));
+    if ((lane & 15) == 0) mbar_arrive(smem_u32(&S.empty[s]));  // the group is done with the warp's two pages
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int rec = 4 * grp + c0 + c;
+      sc[c] = rec < pi.nrows ? sc[c] : kNaNBits;
+      pos[c] = static_cast<uint32_t>(pi.lp * kPage + rec);
+    }
+    return true;
+  };
+
+  uint32_t cur_sc[2] = {0, 0}, cur_pos[2] = {0, 0}, nxt_sc[2] = {0, 0}, nxt_pos[2] = {0, 0};
+  bool ok = stage(0, cur_sc, cur_pos);
+
+  CursorT<kTP> cur;
+  cur.init(P, S.plan);
+  int seg = 0;
+  for (int64_t t = 0; ok && t < nt; ++t) {
+    const bool seg_start = (t == 0) || (cur.lt == 0);
+    if (seg_start && t > 0) ++seg;
+    const bool seg_end = (t == nt - 1) || (cur.lt == cur.tiles - 1);
+    const int qs = seg & 1;
+    if (seg_start) {  // this segment's head weights are in place
+      ok = mbar_wait(smem_u32(&S.qfull[qs]), static_cast<uint32_t>((seg >> 1) & 1), &S.abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    }
+    const float4* wv = reinterpret_cast<const float4*>(S.wbuf[qs]);
+    const uint32_t h = static_cast<uint32_t>(2 * t + gi);  // half-tiles of a CTA stay far below 2^32
+    const int ds = static_cast<int>(h % kDStages);
+    // MMAs of h done: the accumulators are ready and the group's A stage is free
+    ok = mbar_wait(smem_u32(&S.dfull[ds]), (h / kDStages) & 1, &S.abort_flag);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    if (t + 1 < nt) {
+      ok = stage(t + 1, nxt_sc, nxt_pos);
+      if (!ok) break;
+    }
+    tc_fence_after();
+    // logit = s * sum_h relu(x_h) w_h for both records; relu(s x) = |s| relu(sign(s) x)
+    const float s0 = __uint_as_float(cur_sc[0]), s1 = __uint_as_float(cur_sc[1]);
+    const float g0 = s0 < 0.0f ? -1.0f : 1.0f, g1 = s1 < 0.0f ? -1.0f : 1.0f;
+    const bool all_pos = __all_sync(0xFFFFFFFFu, g0 > 0.0f && g1 > 0.0f);
+    const uint32_t tc = tmem + lane_off + d_col(ds);
+    uint64_t acc0[2] = {0ull, 0ull}, acc1[2] = {0ull, 0ull};
+#pragma unroll 1
+    for (int c = 0; c < kH; c += 16) {  // heads c .. c+15 of both records per TMEM wait
+      uint32_t x0[16], x1[16];
+      tmem_ld16(tc + c, x0);
+      tmem_ld16(tc + kH + c, x1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 wq = wv[(c >> 2) + j];
+        const uint64_t w01 = f2pack(wq.x, wq.y), w23 = f2pack(wq.z, wq.w);
+        float a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          a[i] = __uint_as_float(x0[4 * j + i]);
+          b[i] = __uint_as_float(x1[4 * j + i]);
+          if (!all_pos) {
+            a[i] *= g0;
+            b[i] *= g1;
+          }
+        }
+        acc0[0] = f2fma(f2pack(fmaxf(a[0], 0.0f), fmaxf(a[1], 0.0f)), w01, acc0[0]);
+        acc0[1] = f2fma(f2pack(fmaxf(a[2], 0.0f), fmaxf(a[3], 0.0f)), w23, acc0[1]);
+        acc1[0] = f2fma(f2pack(fmaxf(b[0], 0.0f), fmaxf(b[1], 0.0f)), w01, acc1[0]);
+        acc1[1] = f2fma(f2pack(fmaxf(b[2], 0.0f), fmaxf(b[3], 0.0f)), w23, acc1[1]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.dempty[ds]));
+    float logit[2];
+    {
+      float p0, p1, p2, p3;
+      f2unpack(acc0[0], p0, p1);
+      f2unpack(acc0[1], p2, p3);
+      logit[0] = fabsf(s0) * ((p0 + p2) + (p1 + p3));
+      f2unpack(acc1[0], p0, p1);
+      f2unpack(acc1[1], p2, p3);
+      logit[1] = fabsf(s1) * ((p0 + p2) + (p1 + p3));
+    }
+    if constexpr (!kTopk) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        if (!isnan(__uint_as_float(cur_sc[c]))) {
+          const float val = P.raw_logits ? logit[c] : __frcp_rn(1.0f + __expf(-logit[c]));
+          P.scores[static_cast<int64_t>(cur.b) * P.score_stride + cur.lt * kTileRecs + pg_in_tile * kPage + 4 * grp +
+                   c0 + c] = val;
+        }
+    } else {
+      const int slot = static_cast<int>(t % kKeyRing);
+      ok = mbar_wait(smem_u32(&S.kempty[slot]), static_cast<uint32_t>(((t / kKeyRing) & 1) ^ 1), &S.abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      const uint32_t thr = filter_word(S, seg);
+      const uint32_t ltm = lanemask_lt();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const bool valid = !isnan(__uint_as_float(cur_sc[c])) && !isnan(logit[c]);
+        const uint64_t key = valid ? make_key(logit[c], static_cast<int32_t>(cur_pos[c])) : 0ull;
+        const bool take = valid && static_cast<uint32_t>(key >> 32) >= thr;
+        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, take);
+        const int region = 4 * (c0 + c) + q;
+        if (take) S.keys[slot][32 * region + __popc(ballot & ltm)] = key;
+        if (lane == 0) S.kcnt[slot][region] = static_cast<uint32_t>(__popc(ballot));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.kfull[slot]));
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      cur_sc[c] = nxt_sc[c];
+      cur_pos[c] = nxt_pos[c];
+    }
+    if (seg_end) {  // done with this segment's head weights
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.qempty[qs]));
+    }
+    cur.advance(P);
+  }
+}
+
+// ------------------------------------------------------------------ selector
+
+// Same selection as the other scorer, per tile: the tile's admissible keys
+// (16 regions, one per class and worker warp) enter a shared buffer, which is
+// cut back to between k and loose_keep(k) keys when it could overflow; each
+// segment's survivors go to workspace slot (row + CTA).
+__device__ void role_select(const Params& P, Smem& S) {
+  const int g = threadIdx.x - kWarpSelect * 32;
+  const int sw = g >> 5, lane = g & 31;
+  CursorT<kTP> cur;
+  cur.init(P, S.plan);
+  int seg = 0;
+  for (int64_t t = 0; t < S.plan.ntiles; ++t) {
+    const int slot = static_cast<int>(t % kKeyRing);
+    const uint32_t ph = static_cast<uint32_t>((t / kKeyRing) & 1);
+    if (g == 0) S.go[t & 1] = mbar_wait(smem_u32(&S.kfull[slot]), ph, &S.abort_flag) ? 1 : 0;
+    named_bar_sync(kBarSelect, 128);  // passes the leader's acquire of the slot on to the group
+    if (!S.go[t & 1]) break;
+    // The workers kept only keys at or above the published threshold word, so
+    // every key of the tile is appended: region i (class i / 4, lane quarter
+    // i % 4) goes to n + (keys of regions 0 .. i-1). No atomics.
+    {
+      const uint4* kc = reinterpret_cast<const uint4*>(S.kcnt[slot]);
+      uint32_t cnt[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = kc[i];
+        cnt[4 * i] = v.x;
+        cnt[4 * i + 1] = v.y;
+        cnt[4 * i + 2] = v.z;
+        cnt[4 * i + 3] = v.w;
+      }
+      const uint32_t n0 = S.sel.n;
+      uint32_t total = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if ((i & 3) == sw) {  // this warp copies lane quarter sw of every class
+          if (static_cast<uint32_t>(lane) < cnt[i]) S.cand[n0 + total + lane] = S.keys[slot][32 * i + lane];
+        }
+        total += cnt[i];
+      }
+      named_bar_sync(kBarSelect, 128);
+      if (g == 0) S.sel.n = n0 + total;
+    }
+    named_bar_sync(kBarSelect, 128);
+    if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
+    shrink_if_above<128, 128>(S.cand, S.scratch, kCapW - kTileRecs, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+    const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
+    if (seg_end) {
+      shrink_if_above<128, 128>(S.cand, S.scratch, loose_keep(P.k), P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+      const int n = static_cast<int>(S.sel.n);
+      uint8_t* out = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
+      uint64_t* ent = reinterpret_cast<uint64_t*>(out + 16);
+      for (int j = g; j < n; j += 128) ent[j] = S.cand[j];
+      named_bar_sync(kBarSelect, 128);
+      if (g == 0) {
+        *reinterpret_cast<int32_t*>(out) = n;
+        S.sel.n = 0;
+        S.sel.tau = 0;
+      }
+      named_bar_sync(kBarSelect, 128);
+      ++seg;
+    }
+    if (g == 0) {
+      const uint64_t T = S.sel.tau + 1;  // keys >= T are admitted
+      *reinterpret_cast<volatile uint64_t*>(&S.filt) =
+          (static_cast<uint64_t>(static_cast<uint32_t>(seg)) << 32) | static_cast<uint32_t>(S.sel.tau ? T >> 32 : 0);
+    }
+    cur.advance(P);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <bool kTopk>
+__global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = smem_of(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    S.plan.flags = 0;
+    S.abort_flag = 0;
+    S.status = 0;
+    S.sel.n = 0;
+    S.sel.tau = 0;
+    S.filt = ~0ull;  // tagged with no segment: admits everything
+  }
+  __syncthreads();
+  make_plan<kThreads, kTP>(P, &S.plan, S.warp_sums, kTopk ? reinterpret_cast<int32_t*>(P.ws) : nullptr);
+  if (tid == 0 && blockIdx.x == 0 && S.plan.flags && P.dev_status) atomicOr(P.dev_status, S.plan.flags);
+  if (S.plan.ntiles == 0) return;  // uniform
+
+  if (tid == 0) {
+    for (int s = 0; s < kPages; ++s) {
+      mbar_init(smem_u32(&S.full[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), 2);  // the two worker warps (one per group) that read the page
+    }
+    for (int g = 0; g < 2; ++g) mbar_init(smem_u32(&S.afull[g]), 4);  // the four warps of the group
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(smem_u32(&S.dfull[s]), 1);
+      mbar_init(smem_u32(&S.dempty[s]), 4);
+    }
+    for (int i = 0; i < kKeyRing; ++i) {
+      mbar_init(smem_u32(&S.kfull[i]), kWorkerWarps);  // every worker warp, once per tile
+      mbar_init(smem_u32(&S.kempty[i]), 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(&S.rfull[i]), 1);
+      mbar_init(smem_u32(&S.rempty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&S.qfull[i]), 1);
+      mbar_init(smem_u32(&S.qempty[i]), kQEmptyCount);
+    }
+    mbar_init(smem_u32(&S.drain), 1);
+    mbar_init_fence();
+    fence_proxy_async_smem();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  {
+    int32_t qflags = 0;
+    prep_first_query<kH>(P, S, S.plan.b0, &qflags);
+    fence_proxy_async_smem();  // the MMA reads the query through the async proxy
+    if (qflags) atomicOr(&S.status, qflags);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) mbar_arrive(smem_u32(&S.qfull[0]));
+
+  if (warp == kWarpIssuer) {
+    role_issuer(P, S);
+  } else if (warp == kWarpMma) {
+    if ((tid & 31) == 0) role_mma(P, S);
+  } else if (warp == kWarpWalker) {
+    walk_pages<kTP>(P, S);
+  } else if (warp == kWarpQprep) {
+    prep_segments<kH, kTP>(P, S);
+  } else if (warp < kWarpSelect) {
+    role_worker<kTopk>(P, S);
+  } else if (kTopk) {
+    role_select(P, S);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(S.tmem_base, kTmemCols);
+  }
+  if (tid == 0 && P.dev_status) {
+    const int32_t st = S.status | (S.abort_flag ? CSA_DEV_TIMEOUT : 0);
+    if (st) atomicOr(P.dev_status, st);
+  }
+}
+
+}  // namespace w64
+}  // namespace csa
