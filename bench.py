@@ -40,7 +40,7 @@ UNIT = "keys/s"
 K_TOP = 512
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_long_ragged_decode.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "sparse_attention_kv_e4m3_gb300", "csrc", f)
-                  for f in ("csa_index.cu", "csa_ptx.cuh", "csa_select.cuh")]
+                  for f in ("csa_index.cu", "csa_score64.cuh", "csa_ptx.cuh", "csa_select.cuh", "csa_internal.h")]
 
 
 def kernel_source_hash() -> str:
@@ -401,7 +401,7 @@ def run_native(args):
                    "seed": rank},
         "queries_per_s": w.num_q * world / (ms_max / 1e3),
         "gbs": alg_bytes * world / (ms_max / 1e3) / 1e9,
-        "roofline": {"kernel": "score_kernel<topk> (scoring phase)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "w64::score_kernel_w64<topk> (scoring phase)", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "phase1_ms": phase1_ms,
                      "algorithmic_bytes_per_launch": alg_bytes},

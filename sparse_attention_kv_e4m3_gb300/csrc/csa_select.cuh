@@ -49,6 +49,8 @@ struct SelectShared {
   uint64_t tau;       // admission threshold: a key must exceed it
   uint64_t cut[kCutCandidates];        // candidate thresholds of a sampled cut, descending
   uint32_t cut_count[kCutCandidates];  // keys >= each
+  uint32_t part[2][8];                 // per-warp partials of a histogram cut (up to 8 warps)
+  uint32_t pick[3];                    // its boundary bin, keys above it, keys in it
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -288,6 +290,130 @@ __device__ uint64_t cut_sampled(uint64_t* keys, int n, int kk, int max_keep, uin
   return static_cast<uint64_t>(best) << 32;
 }
 
+// Histogram cut with the keys held in registers. Tries to find a value word T
+// with kk <= #(keys[0, n) >= T << 32) <= max_keep and, when it does, compacts
+// those keys in place to the front of `keys`, sets ss->n to their count and
+// ss->tau so that later keys must be >= T << 32, and returns true. Returns false,
+// with `keys` untouched, only when ties of value words make every such T
+// impossible (the caller then selects on whole keys). n <= KPT * NT.
+//
+// Thread g holds keys g, g + NT, ... in registers for the whole cut, so the
+// compaction may overwrite the buffer in any order. The value words span
+// [lo, hi]; a round spreads the words of a window [base, base + 256 * 2^s) over
+// 256 bins of width 2^s, scans the bin counts from the top and finds the bin
+// holding the kk-th key. If every key from that bin up fits in max_keep, the
+// bin's lower edge is T; otherwise the next round zooms into that bin with bins
+// 256 times narrower. Four rounds at most (8 bits each); the first usually
+// decides, because the window starts at the keys' own range.
+template <int NT, int KPT>
+__device__ bool cut_hist(uint64_t* keys, int n, int kk, int max_keep, SelectShared* ss, int bar, int gtid) {
+  static_assert(NT == 128, "two bins per thread");
+  constexpr int NW = NT / 32;
+  const int lane = gtid & 31, warp = gtid >> 5;
+  uint64_t k[KPT];
+  uint32_t lo = 0xFFFFFFFFu, hi = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int i = gtid + NT * j;
+    k[j] = i < n ? keys[i] : 0ull;  // keys are nonzero: 0 marks an empty register
+    if (i < n) {
+      const uint32_t v = static_cast<uint32_t>(k[j] >> 32);
+      lo = min(lo, v);
+      hi = max(hi, v);
+    }
+  }
+  lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (lane == 0) {
+    ss->part[0][warp] = lo;
+    ss->part[1][warp] = hi;
+  }
+  ss->hist[2 * gtid] = 0;
+  ss->hist[2 * gtid + 1] = 0;
+  named_bar_sync(bar, NT);
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, ss->part[0][w]);
+    hi = max(hi, ss->part[1][w]);
+  }
+  uint32_t base = lo;
+  int s = 24 - __clz(hi - lo);  // 256 bins of width 2^s cover [lo, hi]
+  s = s < 0 ? 0 : s;
+  uint32_t need = static_cast<uint32_t>(kk), room = static_cast<uint32_t>(max_keep), T = 0;
+  while (true) {
+    // keys above the window were taken in an earlier round, keys below it dropped
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const uint32_t v = static_cast<uint32_t>(k[j] >> 32);
+      if (k[j] != 0ull && v >= base) {
+        const uint32_t d = (v - base) >> s;
+        if (d < 256u) atomicAdd(&ss->hist[d], 1u);
+      }
+    }
+    named_bar_sync(bar, NT);
+    // thread g reads bins 255 - 2g and 254 - 2g (descending) and clears them for
+    // the next round; the scan below is over those pairs
+    const uint32_t c0 = ss->hist[255 - 2 * gtid], c1 = ss->hist[254 - 2 * gtid];
+    ss->hist[255 - 2 * gtid] = 0;
+    ss->hist[254 - 2 * gtid] = 0;
+    const uint32_t sum = c0 + c1;
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (lane == 31) ss->part[0][warp] = incl;
+    named_bar_sync(bar, NT);
+    uint32_t excl = incl - sum;
+    for (int w = 0; w < warp; ++w) excl += ss->part[0][w];
+    if (excl < need && need <= excl + sum) {  // one thread: the kk-th key is in one of its bins
+      const bool first = need <= excl + c0;
+      ss->pick[0] = first ? 255 - 2 * gtid : 254 - 2 * gtid;
+      ss->pick[1] = first ? excl : excl + c0;
+      ss->pick[2] = first ? c0 : c1;
+    }
+    named_bar_sync(bar, NT);
+    const uint32_t d = ss->pick[0], above = ss->pick[1], cnt = ss->pick[2];
+    if (above + cnt <= room) {
+      T = base + (d << s);
+      break;
+    }
+    if (s == 0) return false;  // uniform: one value word holds too many keys
+    need -= above;
+    room -= above;
+    base += d << s;
+    s = s >= 8 ? s - 8 : 0;
+  }
+  // compaction in place: exclusive scan of each thread's kept count
+  uint32_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) mine += (k[j] != 0ull && static_cast<uint32_t>(k[j] >> 32) >= T) ? 1u : 0u;
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) ss->part[1][warp] = incl;
+  named_bar_sync(bar, NT);
+  uint32_t p = incl - mine, total = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t c = ss->part[1][w];
+    p += w < warp ? c : 0u;
+    total += c;
+  }
+#pragma unroll
+  for (int j = 0; j < KPT; ++j)
+    if (k[j] != 0ull && static_cast<uint32_t>(k[j] >> 32) >= T) keys[p++] = k[j];
+  if (gtid == 0) {
+    ss->n = total;
+    ss->tau = (static_cast<uint64_t>(T) << 32) - 1;  // T >= lo > 0: no value word is 0
+  }
+  return true;
+}
+
 // Every thread offers two keys (`take_a`, `take_b`); accepted keys are appended
 // to buf at ss->n with one shared atomic per warp. The caller's group barrier
 // makes ss->n current.
@@ -337,6 +463,24 @@ __device__ __noinline__ void shrink_if_above(uint64_t* buf, uint64_t* scratch, i
   if (gtid == 0) {
     ss->n = static_cast<uint32_t>(m);
     ss->tau = T ? T - 1 : 0;  // admit keys > T - 1, i.e. >= T; later keys are new (distinct)
+  }
+  named_bar_sync(bar, NT);
+}
+
+// shrink_if_above for a buffer of at most KPT * NT keys: the histogram cut in
+// registers, with the exact radix selection as its fallback.
+template <int NT, int KPT>
+__device__ __noinline__ void shrink_if_above_reg(uint64_t* buf, uint64_t* scratch, int limit, int kk, int max_keep,
+                                                 SelectShared* ss, int bar, int gtid) {
+  const int n = static_cast<int>(ss->n);
+  if (n <= limit || n <= kk) return;
+  if (!cut_hist<NT, KPT>(buf, n, kk, max_keep, ss, bar, gtid)) {
+    const uint64_t T = select_kth<NT>(buf, n, kk, max_keep, ss, bar, gtid);
+    const int m = compact_ge<NT>(buf, n, T, scratch, max_keep, ss, bar, gtid);
+    if (gtid == 0) {
+      ss->n = static_cast<uint32_t>(m);
+      ss->tau = T ? T - 1 : 0;
+    }
   }
   named_bar_sync(bar, NT);
 }
