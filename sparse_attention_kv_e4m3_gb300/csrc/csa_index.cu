@@ -1278,6 +1278,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
     S.sel.n = 0;
     S.sel.tau = 0;
   }
+  // Launched as a programmatic dependent of the scoring kernel, this CTA may
+  // start while that grid still runs: wait here until it has completed and its
+  // slot writes are visible (returns at once after an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // row b's tiles are virtual tiles t0 + W .. t1 - 1 (none when t0 == t1)
   const int64_t t0 = tile_off[b], t1 = tile_off[b + 1], total = tile_off[P.num_q], W = tile_off[P.num_q + 1];
   int64_t c0 = 0, c1 = -1;
@@ -1342,11 +1346,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
     if (tid == 0) S.sel.n = static_cast<uint32_t>(n);
     __syncthreads();
     if (j0 < nslots) {
-      shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, window, P.k, window, &S.sel, 0, tid);
+      shrink_if_above_reg<kMergeThreads, kMergeCap / kMergeThreads>(S.cand, S.scratch, window, P.k, window, &S.sel,
+                                                                    0, tid);
       n = static_cast<int>(S.sel.n);
     }
   }
-  shrink_if_above<kMergeThreads, 256>(S.cand, S.scratch, window, P.k, window, &S.sel, 0, tid);
+  shrink_if_above_reg<kMergeThreads, kMergeCap / kMergeThreads>(S.cand, S.scratch, window, P.k, window, &S.sel, 0,
+                                                                tid);
   n = static_cast<int>(S.sel.n);
   sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
   for (int j = tid; j < P.k; j += kMergeThreads) {
@@ -1664,6 +1670,27 @@ csa_status csa_score_fold(const csa_index_args* args, float* acc, int64_t stride
   return launch_score(args, P, sms, stream);
 }
 
+// Launches the merge right behind the kernel that filled the slots on stream s.
+// When nothing else sits between the two on the stream (pdl), it is a
+// programmatic dependent launch: its CTAs are placed on SMs as the scoring CTAs
+// leave them and wait inside the kernel for the scoring grid to complete, so
+// the launch latency is off the critical path.
+template <bool kFromLogit>
+csa_status launch_merge(const Params& P, int32_t num_q, int32_t* idx, float* vals, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_q));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = sizeof(MergeSmem) + 16;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel<kFromLogit>, P, idx, vals) != cudaSuccess) return CSA_ERR_CUDA;
+  return launch_status();
+}
+
 extern "C" {
 
 csa_status csa_index_score_topk_fused(const csa_index_args* args, int32_t k, int32_t* idx, float* vals, void* ws,
@@ -1692,8 +1719,7 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = launch_w64(P, true, sms, s)) != CSA_OK) return st;
   if (event && cudaEventRecord(static_cast<cudaEvent_t>(event), s) != cudaSuccess) return CSA_ERR_CUDA;
-  merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
-  return launch_status();
+  return launch_merge<true>(P, args->num_q, idx, vals, s, event == nullptr);
 }
 
 csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_index_args* args, int32_t k,
@@ -1722,8 +1748,7 @@ csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   topk_scores_kernel<<<P.grid, kTopkThreads, sizeof(TopkSmem) + 16, s>>>(P);
   if ((st = launch_status()) != CSA_OK) return st;
-  merge_kernel<false><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
-  return launch_status();
+  return launch_merge<false>(P, args->num_q, idx, vals, s, true);
 }
 
 }  // extern "C"
@@ -1782,6 +1807,5 @@ extern "C" csa_status csa_index_score_topk_fused_static(const csa_index_args* ar
   P.grid = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = launch_w64(P, true, sms, s)) != CSA_OK) return st;
-  merge_kernel<true><<<args->num_q, kMergeThreads, sizeof(MergeSmem) + 16, s>>>(P, idx, vals);
-  return launch_status();
+  return launch_merge<true>(P, args->num_q, idx, vals, s, true);
 }

@@ -307,7 +307,8 @@ __device__ uint64_t cut_sampled(uint64_t* keys, int n, int kk, int max_keep, uin
 // decides, because the window starts at the keys' own range.
 template <int NT, int KPT>
 __device__ bool cut_hist(uint64_t* keys, int n, int kk, int max_keep, SelectShared* ss, int bar, int gtid) {
-  static_assert(NT == 128, "two bins per thread");
+  static_assert(NT == 128 || NT == 256, "one or two of the 256 bins per thread");
+  constexpr int BPT = 256 / NT;
   constexpr int NW = NT / 32;
   const int lane = gtid & 31, warp = gtid >> 5;
   uint64_t k[KPT];
@@ -328,8 +329,8 @@ __device__ bool cut_hist(uint64_t* keys, int n, int kk, int max_keep, SelectShar
     ss->part[0][warp] = lo;
     ss->part[1][warp] = hi;
   }
-  ss->hist[2 * gtid] = 0;
-  ss->hist[2 * gtid + 1] = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) ss->hist[BPT * gtid + j] = 0;
   named_bar_sync(bar, NT);
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
@@ -351,12 +352,15 @@ __device__ bool cut_hist(uint64_t* keys, int n, int kk, int max_keep, SelectShar
       }
     }
     named_bar_sync(bar, NT);
-    // thread g reads bins 255 - 2g and 254 - 2g (descending) and clears them for
-    // the next round; the scan below is over those pairs
-    const uint32_t c0 = ss->hist[255 - 2 * gtid], c1 = ss->hist[254 - 2 * gtid];
-    ss->hist[255 - 2 * gtid] = 0;
-    ss->hist[254 - 2 * gtid] = 0;
-    const uint32_t sum = c0 + c1;
+    // thread g reads bins 255 - BPT g - j, j < BPT (descending), and clears them
+    // for the next round; the scan below is over those groups
+    uint32_t c[BPT], sum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      c[j] = ss->hist[255 - BPT * gtid - j];
+      ss->hist[255 - BPT * gtid - j] = 0;
+      sum += c[j];
+    }
     uint32_t incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -368,10 +372,16 @@ __device__ bool cut_hist(uint64_t* keys, int n, int kk, int max_keep, SelectShar
     uint32_t excl = incl - sum;
     for (int w = 0; w < warp; ++w) excl += ss->part[0][w];
     if (excl < need && need <= excl + sum) {  // one thread: the kk-th key is in one of its bins
-      const bool first = need <= excl + c0;
-      ss->pick[0] = first ? 255 - 2 * gtid : 254 - 2 * gtid;
-      ss->pick[1] = first ? excl : excl + c0;
-      ss->pick[2] = first ? c0 : c1;
+      uint32_t acc = excl;
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) {
+        if (acc < need && need <= acc + c[j]) {
+          ss->pick[0] = 255 - BPT * gtid - j;
+          ss->pick[1] = acc;
+          ss->pick[2] = c[j];
+        }
+        acc += c[j];
+      }
     }
     named_bar_sync(bar, NT);
     const uint32_t d = ss->pick[0], above = ss->pick[1], cnt = ss->pick[2];
