@@ -25,25 +25,33 @@
 // more), so each head's column holds k . (q * 2^e_h) itself. A half-tile is two
 // class sub-tiles (classes 2g and 2g + 1 of a tile) and belongs to worker group
 // g; a worker lane then carries two records per iteration, which amortises the
-// iteration's fixed barrier and hand-off latencies. The MMA warp issues a
-// half-tile's 16 MMAs back to back from precomputed operands: measured here, a
-// thread issues at most one tcgen05.mma every ~50 cycles in a tight loop (and
-// two issuing warps reach the tensor pipe's ~32 cycles per N=64 MMA), while a
-// loop that rebuilds descriptors and branches per MMA takes ~95-106.
+// iteration's fixed barrier and hand-off latencies. Two threads in two warps
+// issue the MMAs, one class sub-tile of each half-tile each (8 MMAs back to
+// back from precomputed operands), and both commit to the half-tile's
+// accumulator-ready barrier: measured here, one thread issues at most one
+// tcgen05.mma every ~50 cycles in a tight loop (~80 beside the busy warps of
+// its scheduler), two issuing warps reach the tensor pipe's ~32 cycles per N=64
+// MMA, and a loop that rebuilds descriptors and branches per MMA takes ~95-106.
 //
 // Warp roles (512 threads):
 //   0      issuer: 8 lanes in lockstep, one 1-D bulk copy per page into a ring of
 //          kPages slots
-//   1      MMA (one thread); allocates the 512 TMEM columns
+//   1      MMA issue for class sub-tiles 0 and 2 (one thread); allocates the
+//          512 TMEM columns
 //   2      page walker (shared with the other scorer)
-//   3      query preparation for the CTA's later segments (the first is split
-//          by the whole CTA in the prologue); two query slots
+//   3      MMA issue for class sub-tiles 1 and 3 (one thread)
 //   4-11   workers, two groups of four (one warp per TMEM lane quarter): group
 //          g owns classes 2g and 2g + 1 of every tile. For each tile: wait for
 //          the MMAs of its half-tile, stage the next tile's half-tile into the
 //          group's TMEM A stage (its MMAs then overlap), then the epilogue of
 //          both records.
-//   12-15  selector (top-k mode): one tile of keys (all four classes) per step
+//   12-15  selector (top-k mode): one tile of keys (all four classes) per step;
+//          also splits the queries of the CTA's later segments (the first is
+//          split by the whole CTA in the prologue; two query slots), 16 heads
+//          per warp: segment s + 2's into the slot of segment s once it has
+//          taken s's last keys, by which time the MMAs and the epilogues of s
+//          are done. In score mode warp 12 prepares them instead, each as soon
+//          as the MMAs and the workers release its slot.
 //
 // TMEM: one 64-column A stage per worker group (columns 0 and 64: two class
 // sub-tiles of 32 columns) and three 128-column accumulator stages (columns
@@ -64,10 +72,10 @@ constexpr int kDStages = 3;                          // accumulator stages
 constexpr int kKeyRing = 4;                          // tiles of keys, workers -> selector
 constexpr int kCapW = 2048;                          // candidate buffer of one segment
 constexpr int kThreads = 512;
-constexpr int kWarpIssuer = 0, kWarpMma = 1, kWarpWalker = 2, kWarpQprep = 3, kWarpWorker = 4, kWarpSelect = 12;
+constexpr int kWarpIssuer = 0, kWarpMma = 1, kWarpWalker = 2, kWarpMma2 = 3, kWarpWorker = 4, kWarpSelect = 12;
 constexpr int kWorkerWarps = 8;
 constexpr int kBarSelect = 1;
-constexpr int kQEmptyCount = 1 + kWorkerWarps;       // MMA commit + every worker warp
+constexpr int kQEmptyCount = 2 + kWorkerWarps;       // both MMA threads' commits + every worker warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, kH);
 
@@ -199,7 +207,10 @@ __device__ void role_issuer(const Params& P, Smem& S) {
 
 // ------------------------------------------------------------------ MMA
 
-__device__ void role_mma(const Params& P, Smem& S) {
+// One of the two issuing threads: class sub-tile c of every half-tile (classes
+// c and 2 + c of each tile). Both commit to the half-tile's accumulator-ready
+// barrier, to the query slot's release at a segment end and to the final drain.
+__device__ void role_mma(const Params& P, Smem& S, const int c) {
   CursorT<kTP> cur;
   cur.init(P, S.plan);
   const uint32_t tmem = S.tmem_base;
@@ -225,14 +236,11 @@ __device__ void role_mma(const Params& P, Smem& S) {
            mbar_wait(smem_u32(&S.dempty[ds]), ((h / kDStages) & 1) ^ 1, &S.abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d = tmem + d_col(ds), a = tmem + a_col(g);
+      const uint32_t d = tmem + d_col(ds) + kH * c, a = tmem + a_col(g) + 32 * c;
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+      for (int term = 0; term < 2; ++term)
 #pragma unroll
-        for (int term = 0; term < 2; ++term)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_e4m3_ts(d + kH * c, a + 32 * c + 8 * kk, bdesc[term][kk], kIdesc, (term | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk) mma_e4m3_ts(d, a + 8 * kk, bdesc[term][kk], kIdesc, (term | kk) != 0);
       mma_commit(smem_u32(&S.dfull[ds]));
     }
     if (!ok) break;
@@ -443,6 +451,46 @@ __device__ void role_worker(const Params& P, Smem& S) {
 
 // ------------------------------------------------------------------ selector
 
+// Splits heads h0 .. h0 + 15 of query row b into query slot qs (one warp): the
+// arithmetic and layout of prep_query over a quarter of the heads, with all 16
+// heads' loads in flight at once.
+__device__ void prep_query_part(const Params& P, Smem& S, int32_t b, int qs, int h0, int32_t* flags) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t* qrow = P.q + (static_cast<int64_t>(b) * kH + h0) * kD;
+  const float w_mine = lane < 16 ? __ldg(P.w + static_cast<int64_t>(b) * kH + h0 + lane) : 0.0f;
+  uint8_t* hi = S.qbuf[qs][0];
+  uint8_t* lo = S.qbuf[qs][1];
+  uint2 raw[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) raw[j] = __ldg(reinterpret_cast<const uint2*>(qrow + j * kD + lane * 4));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int h = h0 + j;
+    float x[4];
+    x[0] = __uint_as_float(raw[j].x << 16);
+    x[1] = __uint_as_float(raw[j].x & 0xFFFF0000u);
+    x[2] = __uint_as_float(raw[j].y << 16);
+    x[3] = __uint_as_float(raw[j].y & 0xFFFF0000u);
+    float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float sc, isc;
+    head_scale(m, flags, &sc, &isc);
+    uint32_t whi = 0, wlo = 0;
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      uint32_t h2, l2;
+      split_pair(x[2 * pr] * sc, x[2 * pr + 1] * sc, &h2, &l2);
+      whi |= h2 << (16 * pr);
+      wlo |= l2 << (16 * pr);
+    }
+    const uint32_t off = qbuf_offset(h, lane >> 2) + (lane & 3) * 4;
+    *reinterpret_cast<uint32_t*>(hi + off) = whi;
+    *reinterpret_cast<uint32_t*>(lo + off) = wlo;
+    if (lane == j) S.wbuf[qs][h] = w_mine * isc;
+  }
+}
+
 // Same selection as the other scorer, per tile: the tile's admissible keys
 // (16 regions, one per class and worker warp) enter a shared buffer, which is
 // cut back to between k and loose_keep(k) keys when it could overflow; each
@@ -453,6 +501,24 @@ __device__ void role_select(const Params& P, Smem& S) {
   CursorT<kTP> cur;
   cur.init(P, S.plan);
   int seg = 0;
+  // query preparation: the next segment to prepare (1, then 2, ...), its row,
+  // and the tiles that the segments prepared so far cover
+  int32_t qflags = 0;
+  int prep_seg = 1;
+  int64_t prep_done = query_tiles<kTP>(P, S.plan.b0) - S.plan.lt0;
+  int32_t prep_b = next_nonempty<kTP>(P, S.plan.b0 + 1);
+  auto prep_next = [&]() {
+    if (prep_done >= S.plan.ntiles) return;  // uniform
+    const int qs = prep_seg & 1;
+    prep_query_part(P, S, prep_b, qs, 16 * sw, &qflags);
+    fence_proxy_async_smem();  // the MMA reads the query through the async proxy
+    named_bar_sync(kBarSelect, 128);
+    if (g == 0) mbar_arrive(smem_u32(&S.qfull[qs]));
+    prep_done += query_tiles<kTP>(P, prep_b);
+    prep_b = next_nonempty<kTP>(P, prep_b + 1);
+    ++prep_seg;
+  };
+  prep_next();  // segment 1 into the free slot 1
   for (int64_t t = 0; t < S.plan.ntiles; ++t) {
     const int slot = static_cast<int>(t % kKeyRing);
     const uint32_t ph = static_cast<uint32_t>((t / kKeyRing) & 1);
@@ -503,6 +569,9 @@ __device__ void role_select(const Params& P, Smem& S) {
       }
       named_bar_sync(kBarSelect, 128);
       ++seg;
+      // the keys of segment seg - 1's last tile are in: its MMAs and epilogues
+      // are done with query slot (seg - 1) & 1, which segment seg + 1 takes
+      if (prep_seg == seg + 1) prep_next();
     }
     if (g == 0) {
       const uint64_t T = S.sel.tau + 1;  // keys >= T are admitted
@@ -511,6 +580,7 @@ __device__ void role_select(const Params& P, Smem& S) {
     }
     cur.advance(P);
   }
+  if (qflags) atomicOr(&S.status, qflags);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -540,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
     }
     for (int g = 0; g < 2; ++g) mbar_init(smem_u32(&S.afull[g]), 4);  // the four warps of the group
     for (int s = 0; s < kDStages; ++s) {
-      mbar_init(smem_u32(&S.dfull[s]), 1);
+      mbar_init(smem_u32(&S.dfull[s]), 2);  // both MMA threads commit
       mbar_init(smem_u32(&S.dempty[s]), 4);
     }
     for (int i = 0; i < kKeyRing; ++i) {
@@ -555,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
       mbar_init(smem_u32(&S.qfull[i]), 1);
       mbar_init(smem_u32(&S.qempty[i]), kQEmptyCount);
     }
-    mbar_init(smem_u32(&S.drain), 1);
+    mbar_init(smem_u32(&S.drain), 2);
     mbar_init_fence();
     fence_proxy_async_smem();
   }
@@ -577,15 +647,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
   if (warp == kWarpIssuer) {
     role_issuer(P, S);
   } else if (warp == kWarpMma) {
-    if ((tid & 31) == 0) role_mma(P, S);
+    if ((tid & 31) == 0) role_mma(P, S, 0);
+  } else if (warp == kWarpMma2) {
+    if ((tid & 31) == 0) role_mma(P, S, 1);
   } else if (warp == kWarpWalker) {
     walk_pages<kTP>(P, S);
-  } else if (warp == kWarpQprep) {
-    prep_segments<kH, kTP>(P, S);
   } else if (warp < kWarpSelect) {
     role_worker<kTopk>(P, S);
   } else if (kTopk) {
     role_select(P, S);
+  } else if (warp == kWarpSelect) {
+    prep_segments<kH, kTP>(P, S);
   }
 
   tc_fence_before();
