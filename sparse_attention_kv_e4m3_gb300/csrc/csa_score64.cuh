@@ -525,31 +525,40 @@ __device__ void role_select(const Params& P, Smem& S) {
     if (g == 0) S.go[t & 1] = mbar_wait(smem_u32(&S.kfull[slot]), ph, &S.abort_flag) ? 1 : 0;
     named_bar_sync(kBarSelect, 128);  // passes the leader's acquire of the slot on to the group
     if (!S.go[t & 1]) break;
-    // The workers kept only keys at or above the published threshold word, so
-    // every key of the tile is appended: region i (class i / 4, lane quarter
-    // i % 4) goes to n + (keys of regions 0 .. i-1). No atomics.
+    // The workers kept the keys at or above the threshold word they last read;
+    // the selector's own threshold may have risen since (a cut that finished
+    // after they read it: they run up to kKeyRing tiles ahead), so every key is
+    // checked again on the way in. Warp sw takes lane quarter sw of each class
+    // (regions 4c + sw) and places its survivors after those of warps 0 .. sw-1.
     {
-      const uint4* kc = reinterpret_cast<const uint4*>(S.kcnt[slot]);
-      uint32_t cnt[16];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = kc[i];
-        cnt[4 * i] = v.x;
-        cnt[4 * i + 1] = v.y;
-        cnt[4 * i + 2] = v.z;
-        cnt[4 * i + 3] = v.w;
-      }
+      const uint64_t tau = S.sel.tau;  // keys must exceed it; 0 at a segment start
       const uint32_t n0 = S.sel.n;
-      uint32_t total = 0;
+      uint64_t key[4];
+      uint32_t bal[4], mine = 0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if ((i & 3) == sw) {  // this warp copies lane quarter sw of every class
-          if (static_cast<uint32_t>(lane) < cnt[i]) S.cand[n0 + total + lane] = S.keys[slot][32 * i + lane];
-        }
-        total += cnt[i];
+      for (int c = 0; c < 4; ++c) {
+        const int i = 4 * c + sw;
+        const bool have = static_cast<uint32_t>(lane) < S.kcnt[slot][i];
+        key[c] = have ? S.keys[slot][32 * i + lane] : 0ull;
+        bal[c] = __ballot_sync(0xFFFFFFFFu, have && key[c] > tau);
+        mine += static_cast<uint32_t>(__popc(bal[c]));
       }
+      if (lane == 0) S.sel.part[0][sw] = mine;
       named_bar_sync(kBarSelect, 128);
-      if (g == 0) S.sel.n = n0 + total;
+      uint32_t off = n0, total = n0;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t c = S.sel.part[0][w];
+        off += w < sw ? c : 0u;
+        total += c;
+      }
+      const uint32_t ltm = lanemask_lt();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if ((bal[c] >> lane) & 1u) S.cand[off + __popc(bal[c] & ltm)] = key[c];
+        off += static_cast<uint32_t>(__popc(bal[c]));
+      }
+      if (g == 0) S.sel.n = total;
     }
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
