@@ -21,7 +21,11 @@
  *   data on the host; all work is enqueued on `stream` (a cudaStream_t passed as
  *   void*, NULL = legacy default stream). The only state it keeps is a one-time
  *   per-device kernel attribute set-up (dynamic shared memory size) and the
- *   device's SM count; both are taken on the first call on a device.
+ *   device's SM count; both are taken on the first call on a device and kept for
+ *   the life of the process (as is the built-in scratch address of
+ *   csa_index_score_topk_fused_static). The library must therefore not be used on
+ *   a device across cudaDeviceReset: the kept state would describe the old
+ *   context.
  * - Calls are re-entrant and capturable in a CUDA graph as long as their
  *   workspaces do not overlap while in flight.
  * - Host-detectable errors return a csa_status and launch nothing.
@@ -231,7 +235,8 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
  *
  * The first call on a device looks up the array's device address for that
  * device (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture. Every call on a device uses the same array and
+ * before any stream capture, and do not use the library across a cudaDeviceReset
+ * of that device (the address is kept). Every call on a device uses the same array and
  * leaves its contents behind; nothing in it has to start at zero, because each
  * call writes every byte it later reads. Calls whose kernels overlap on the GPU
  * (two streams, or two host threads) race on the array and must be serialised

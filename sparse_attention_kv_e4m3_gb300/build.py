@@ -49,6 +49,27 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+# Test builds: the same sources with compile-time switches that only tests use
+# (for example a short pipeline wait limit and a delayed producer, to exercise
+# the bounded-wait path). Each goes to its own file next to the product library.
+TEST_VARIANTS = {
+    "timeout": ["-DCSA_TEST_WAIT_LIMIT_NS=20000ull", "-DCSA_TEST_WALKER_DELAY_NS=200000ull"],
+}
+
+
+def build_test_variant(name: str, force: bool = False) -> str:
+    """Compiles test variant `name` (see TEST_VARIANTS) unless up to date. Returns its path."""
+    path = os.path.join(PKG, f"libcsa_index_test_{name}.so")
+    if not force and os.path.exists(path) and all(os.path.getmtime(d) <= os.path.getmtime(path) for d in DEPS):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = [nvcc_path(), ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+           f"-I{INCLUDE}", "-o", tmp] + TEST_VARIANTS[name] + SOURCES
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
 if __name__ == "__main__":
     import sys
 

@@ -495,6 +495,15 @@ __device__ void walk_pages(const Params& P, SM& S) {
   CursorT<TP> cur;
   cur.init(P, S.plan);
   int32_t flags = 0;
+#ifdef CSA_TEST_WALKER_DELAY_NS
+  // Test build only: the walker publishes nothing for this long, so that the
+  // roles waiting on it run out of their (shortened) wait limit.
+  if (lane == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < CSA_TEST_WALKER_DELAY_NS) __nanosleep(1000);
+  }
+  __syncwarp();
+#endif
   for (int64_t pg = 0; pg < npg; pg += 32) {
     const int64_t batch = pg >> 5;
     const int slot = static_cast<int>(batch % kRing);
@@ -650,9 +659,13 @@ __device__ void role_mma(const Params& P, Smem<H>& S) {
   mbar_wait_drain(smem_u32(&S.drain), 0);
 }
 
-// Per-head power-of-two scale sc (and 1 / sc) mapping the head's largest |q|,
-// m, into (224, 448]; a non-finite m is flagged and treated as 1.
-__device__ __forceinline__ void head_scale(float m, int32_t* flags, float* sc, float* isc) {
+// Per-head power-of-two scale 2^e (and 1 / 2^e) mapping the head's largest |q|,
+// m, into (224, 448] for every finite bf16 m, subnormals included (2^-133 up to
+// 2^128): e runs from -120 to 141. 2^e above 2^126 is not an fp32 value, so the
+// scale is returned as two factors, sc * sc2 (sc2 = 1 unless e > 126), which a
+// value is multiplied by in turn (each product exact); 1 / 2^e is then an fp32
+// subnormal, still exact. A non-finite m is flagged and treated as 1.
+__device__ __forceinline__ void head_scale(float m, int32_t* flags, float* sc, float* sc2, float* isc) {
   if (!isfinite(m)) {
     *flags |= CSA_DEV_RANGE;
     m = 1.0f;
@@ -660,9 +673,11 @@ __device__ __forceinline__ void head_scale(float m, int32_t* flags, float* sc, f
   int E2;
   const float f = frexpf(m, &E2);
   int e = (f <= 0.875f) ? 9 - E2 : 8 - E2;
-  e = e < -126 ? -126 : (e > 126 ? 126 : e);
-  *sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-  *isc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  e = e < -126 ? -126 : (e > 141 ? 141 : e);
+  const int e1 = e > 126 ? 126 : e;
+  *sc = __uint_as_float(static_cast<uint32_t>(e1 + 127) << 23);
+  *sc2 = __uint_as_float(static_cast<uint32_t>(e - e1 + 127) << 23);
+  *isc = e <= 126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : __uint_as_float(1u << (149 - e));
 }
 
 // e4m3 hi and lo terms of two scaled query values (a in the low byte of each):
@@ -737,13 +752,13 @@ __device__ void prep_query(const Params& P, SM& S, int32_t b, int qs, int32_t* f
       float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      float sc, isc;
-      head_scale(m, flags, &sc, &isc);
+      float sc, sc2, isc;
+      head_scale(m, flags, &sc, &sc2, &isc);
       uint32_t whi = 0, wlo = 0;
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr) {
         uint32_t h2, l2;
-        split_pair(x[2 * pr] * sc, x[2 * pr + 1] * sc, &h2, &l2);
+        split_pair(x[2 * pr] * sc * sc2, x[2 * pr + 1] * sc * sc2, &h2, &l2);
         whi |= h2 << (16 * pr);
         wlo |= l2 << (16 * pr);
       }
@@ -788,14 +803,14 @@ __device__ void prep_first_query(const Params& P, SM& S, int32_t b, int32_t* fla
   for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
 #pragma unroll
   for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));  // the head's 8 threads
-  float sc, isc;
-  head_scale(m, flags, &sc, &isc);
+  float sc, sc2, isc;
+  head_scale(m, flags, &sc, &sc2, &isc);
   uint32_t whi[4], wlo[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t h0, l0, h1, l1;
-    split_pair(x[4 * i] * sc, x[4 * i + 1] * sc, &h0, &l0);
-    split_pair(x[4 * i + 2] * sc, x[4 * i + 3] * sc, &h1, &l1);
+    split_pair(x[4 * i] * sc * sc2, x[4 * i + 1] * sc * sc2, &h0, &l0);
+    split_pair(x[4 * i + 2] * sc * sc2, x[4 * i + 3] * sc * sc2, &h1, &l1);
     whi[i] = h0 | (h1 << 16);
     wlo[i] = l0 | (l1 << 16);
   }

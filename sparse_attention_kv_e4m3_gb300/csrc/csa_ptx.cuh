@@ -86,6 +86,19 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
 // raises the CTA's abort flag and reports a timeout instead of hanging.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
+// The limit of the pipeline waits (mbar_wait). A test build of the library
+// (CSA_TEST_WAIT_LIMIT_NS, never the product build) shortens it so that a test
+// can make a wait run out without a long stall; the drains of in-flight copies
+// and MMAs before a CTA exits (mbar_wait_drain) keep the full limit, so no CTA
+// leaves with work outstanding.
+#ifdef CSA_TEST_WAIT_LIMIT_NS
+constexpr uint64_t kPipeWaitLimitNs = CSA_TEST_WAIT_LIMIT_NS;
+constexpr uint32_t kPipeProbesPerClockCheck = 1;
+#else
+constexpr uint64_t kPipeWaitLimitNs = kWaitLimitNs;
+constexpr uint32_t kPipeProbesPerClockCheck = 256;
+#endif
+
 // Probes between two looks at the clock in the bounded waits: a wait that
 // completes within the first probes never reads %globaltimer. A probe lasts at
 // most the suspend hint, so the clock is read at least every 256 x 20 us.
@@ -100,12 +113,12 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait_suspend(bar, parity)) return true;
-    if (++spins % kProbesPerClockCheck == 0) {
+    if (++spins % kPipeProbesPerClockCheck == 0) {
       if (*abort_flag) return false;
       const uint64_t now = globaltimer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > kPipeWaitLimitNs) {
         *abort_flag = 1;
         return false;
       }

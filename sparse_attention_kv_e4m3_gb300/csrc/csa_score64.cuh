@@ -474,13 +474,13 @@ __device__ void prep_query_part(const Params& P, Smem& S, int32_t b, int qs, int
     float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    float sc, isc;
-    head_scale(m, flags, &sc, &isc);
+    float sc, sc2, isc;
+    head_scale(m, flags, &sc, &sc2, &isc);
     uint32_t whi = 0, wlo = 0;
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr) {
       uint32_t h2, l2;
-      split_pair(x[2 * pr] * sc, x[2 * pr + 1] * sc, &h2, &l2);
+      split_pair(x[2 * pr] * sc * sc2, x[2 * pr + 1] * sc * sc2, &h2, &l2);
       whi |= h2 << (16 * pr);
       wlo |= l2 << (16 * pr);
     }

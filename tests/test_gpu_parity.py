@@ -83,6 +83,37 @@ def test_query_split_is_exact_for_large_dynamic_range():
     check_all(w, 100)
 
 
+def test_query_heads_at_the_bottom_of_bf16():
+    """Heads whose largest |q| lies between bf16's smallest subnormal (2^-133)
+    and 2^-126: their power-of-two scale exceeds 2^126 (two factors in the
+    kernel) and the folded weight 2^-e is an fp32 subnormal. With weights of
+    2^100 the logits are of order 2^-20; they must match the oracle to fp32
+    accumulation accuracy, which a split that lost the small heads' low bits
+    (or their subnormal elements) would not."""
+    w = synth.make_workload("tinyq", num_q=2, history=[300, 200], seed=22)
+    rng = np.random.default_rng(5)
+    qf = rng.standard_normal((2, 64, D)).astype(np.float64)
+    top = rng.integers(-133, -125, size=(2, 64, 1)).astype(np.float64)  # each head's largest |q|: 2^top
+    qf = qf / np.abs(qf).max(axis=2, keepdims=True) * 2.0 ** top
+    qf[0, 0, :] = 0.0
+    qf[0, 0, 5] = 2.0 ** -133  # one head holding a single smallest subnormal
+    w.q[:] = _pins.bf16_bits(qf.astype(np.float32))
+    w.fused_w[:] = np.float32(2.0 ** 100) * np.sign(rng.standard_normal((2, 64))).astype(np.float32)
+    prob = native.Problem.from_workload(w)
+    lg = native.csa_index_logits(prob).cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    assert int(prob.dev_status.item()) == 0
+    o_lg, valid, _ = oracle.logits(oracle.Problem(w), lg.shape[1])
+    for b in range(w.num_q):
+        v = valid[b]
+        ref = o_lg[b, v]
+        scale = np.abs(ref).max()
+        assert scale > 2.0 ** -40, "the test must produce visible logits"
+        assert np.max(np.abs(lg[b, v] - ref)) <= 2.0 ** -16 * scale, np.max(np.abs(lg[b, v] - ref)) / scale
+    r = run(w, 64, score=False, unfused=False)
+    _parity.check_topk(w, r["idx"], r["vals"], 64)
+
+
 # ------------------------------------------------------------------ small workloads
 
 SMALL = {

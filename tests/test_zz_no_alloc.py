@@ -79,3 +79,41 @@ def test_rejects_requests_beyond_the_builtin_scratch(lib):
     st = lib.csa_index_score_topk_fused_static(ctypes.byref(a), 512, idx.data_ptr(), idx.data_ptr(),
                                                torch.cuda.current_stream().cuda_stream)
     assert st == CSA_ERR_WORKSPACE
+
+
+def _static_need(num_q: int, k: int, sms: int) -> int:
+    """The header's bound for csa_index_score_topk_fused_static, written out:
+    256-byte-rounded 4 * (num_q + 2), plus (num_q + SMs) slots of
+    16 + 8 * min(1024, k + k / 2) bytes rounded up to 16."""
+    head = (4 * (num_q + 2) + 255) // 256 * 256
+    slot = (16 + 8 * min(1024, k + k // 2) + 15) // 16 * 16
+    return head + (num_q + sms) * slot
+
+
+@pytest.mark.parametrize("k", [512, 1024])
+def test_largest_request_that_fits_the_builtin_scratch(lib, k):
+    """At the largest num_q the bound accepts on this GPU the call must run and
+    match the workspace entry point exactly (the kernel writes slots up to
+    num_q - 1 + grid - 1); one more row must be refused before anything runs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    limit = (4 << 20)
+    nq = 1
+    while _static_need(nq + 1, k, sms) <= limit:
+        nq += 1
+    assert _static_need(nq, k, sms) <= limit < _static_need(nq + 1, k, sms)
+    rng = np.random.default_rng(60 + k)
+    hist = rng.integers(1, 3 * 64, size=nq).tolist()
+    w = synth.make_workload("edge%d" % k, num_q=nq, history=hist, seed=61)
+    prob = native.Problem.from_workload(w)
+    ref_idx, ref_vals = native.csa_index_score_topk_fused(prob, k)
+    idx, vals = _static_call(lib, prob, k)
+    torch.cuda.synchronize()
+    assert int(prob.dev_status.item()) == 0
+    assert torch.equal(idx, ref_idx) and torch.equal(vals, ref_vals)
+    # one row more: refused before launching (the pointers are never read)
+    a = prob.args()
+    a.num_q = nq + 1
+    a.num_req = max(a.num_req, nq + 1)
+    st = lib.csa_index_score_topk_fused_static(ctypes.byref(a), k, idx.data_ptr(), vals.data_ptr(),
+                                               torch.cuda.current_stream().cuda_stream)
+    assert st == CSA_ERR_WORKSPACE
