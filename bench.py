@@ -93,6 +93,85 @@ def algorithmic_bytes(w) -> int:
                + w.num_q * (64 * 128 * 2 + 64 * 4 + 4 + K_TOP * 8))
 
 
+HEADS, HEAD_DIM = 64, 128
+PER_CONFIG = ("tiny_decode", "decode_batch", "resident_1m", "prefill_chunk")
+
+
+def algorithmic_flops(w) -> int:
+    """The contraction's FLOPs: 2 * H * D per (query, visible record), the cost
+    model the pages' per-token FLOP figures follow (FlashMemory-DeepSeek-V4,
+    "Per-decode-token FLOPs (whole model)"); the relu, head weights and
+    sigmoid (about 3H operations per pair) are not counted."""
+    return int(2 * HEADS * HEAD_DIM * int(w.visible_counts().sum()))
+
+
+def indexer_gflop(layers: int, records_per_query: int, heads: int = HEADS, dim: int = HEAD_DIM) -> float:
+    """GFLOP of scoring one decode token's query against `records_per_query`
+    records in each of `layers` indexer layers, at 2 * heads * dim per pair."""
+    return layers * records_per_query * 2.0 * heads * dim / 1e9
+
+
+def measured_peak_tflops():
+    """(dense bf16 TFLOP/s sustained, its source), from MEASURED_PEAKS.json."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured bf16_tflops_sustained"
+    except Exception:
+        return 1700.0, "fallback bf16 sustained"
+
+
+def measure_configs(names, dev, steps: int = 20):
+    """The other configs of the indexer, one fused score + top-512 call each:
+    the median of `steps` event-timed calls, with L2 flushed (a 256 MB write,
+    outside the timed region) before every call, since most of these inputs fit
+    in the 129 MB L2. Reports us per call, keys/s, GB/s of algorithmic bytes and
+    its fraction of the measured copy bandwidth, TFLOP/s of the contraction, and
+    for chunked prefill (the contraction-dense config) the fraction of the dense
+    e4m3 tensor peak, taken as twice the measured sustained bf16 figure (the
+    nominal e4m3 : bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
+    import torch
+    from sparse_attention_kv_e4m3_gb300 import native, synth
+
+    hbm, hbm_src = measured_peaks()
+    bf16, bf16_src = measured_peak_tflops()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name in names:
+        w = synth.config(name)
+        prob = native.Problem.from_workload(w, device=dev)
+        ws = native.alloc_workspace(prob, K_TOP, dev)
+        idx = torch.empty((w.num_q, K_TOP), dtype=torch.int32, device=dev)
+        vals = torch.empty((w.num_q, K_TOP), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            native.csa_index_score_topk_fused(prob, K_TOP, ws, idx, vals, stream=stream)
+        torch.cuda.synchronize(dev)
+        if int(prob.dev_status.item()) != 0:
+            raise RuntimeError(f"{name}: device status {int(prob.dev_status.item())}")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            native.csa_index_score_topk_fused(prob, K_TOP, ws, idx, vals, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        keys, nbytes, flops = int(w.visible_counts().sum()), algorithmic_bytes(w), algorithmic_flops(w)
+        rec = {"us": ms * 1e3, "queries": w.num_q, "records": keys, "keys_per_s": keys / (ms / 1e3),
+               "gbs": nbytes / (ms / 1e3) / 1e9, "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
+               "algorithmic_bytes": nbytes, "flops": flops, "tflops": flops / (ms / 1e3) / 1e12}
+        if name.startswith("prefill"):
+            rec["tensor_frac"] = rec["tflops"] / (2.0 * bf16)
+            rec["tensor_peak"] = f"2 x {bf16} TFLOP/s ({bf16_src}, e4m3 at the nominal 2:1 ratio)"
+        out[name] = rec
+        del prob, ws, idx, vals
+        torch.cuda.empty_cache()
+    out["timing"] = (f"median of {steps} calls, L2 flushed before each; peaks: {hbm} GB/s ({hbm_src})")
+    return out
+
+
 # ---------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -415,7 +494,25 @@ def run_native(args):
         "gpu_launches": 2 * args.steps,
         "device_status": status,
         "wall_s": wall,
+        "flops_per_step": algorithmic_flops(w),
+        "tflops": algorithmic_flops(w) * world / (ms_max / 1e3) / 1e12,
+        # the same 2*H*D-per-pair model applied to the pages' 1M-context decode
+        # token (21 indexer layers; full history vs KMAX=384 resident pages plus
+        # the Level-1 retriever's 3 layers at H=128 every 64 tokens)
+        "cost_model_gflop_per_token_1m": {
+            "full_history_scoring": indexer_gflop(21, 262144),
+            "resident_scoring_and_level1": indexer_gflop(21, 384 * 64) + indexer_gflop(3, 262144, heads=128) / 64},
     }
+    if rank == 0 and world == 1 and not args.no_per_config:
+        line["per_config"] = measure_configs(PER_CONFIG, dev)
+        # the next-row kernels on the same workload's geometry (their own lines:
+        # bench.py --op write_keys / --op recall)
+        extra_args = argparse.Namespace(**{**vars(args), "steps": min(args.steps, 200)})
+        for op, fn in (("write_keys", run_write_keys), ("recall", run_recall)):
+            r = fn(extra_args, emit=False)
+            line[op] = {"metric": r["metric"], "value": r["value"], "unit": r["unit"], "ms_per_step": r["ms_per_step"],
+                        "gbs": r["roofline"]["achieved"], "frac": r["roofline"]["frac"],
+                        "device_status": r["device_status"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, dt, threads, sample = oracle_rate(w, budget_s=10.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -428,7 +525,7 @@ def run_native(args):
     return 0
 
 
-def run_write_keys(args):
+def run_write_keys(args, emit: bool = True):
     """The compressed-K writer on the workload's cache geometry: every visible
     record of every request rewritten from bf16 rows (one row per record)."""
     import torch
@@ -511,11 +608,12 @@ def run_write_keys(args):
         "gpu_launches": steps,
         "device_status": int(status.item()),
     }
-    print(json.dumps(line))
-    return 0
+    if emit:
+        print(json.dumps(line))
+    return line
 
 
-def run_recall(args):
+def run_recall(args, emit: bool = True):
     """Level-1 recall over `--layers` target layers of the workload's history
     (each layer its own device copy of the cache and its own 128-head query):
     every visible record scored per layer, combined by max, thresholded, with the
@@ -620,8 +718,9 @@ def run_recall(args):
         "device_status": int(p0.dev_status.item()),
         "resident_pages_mean": float(npg.float().mean().item()),
     }
-    print(json.dumps(line))
-    return 0
+    if emit:
+        print(json.dumps(line))
+    return line
 
 
 def main():
@@ -632,6 +731,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="long_ragged_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other configs' measurements")
     ap.add_argument("--op", default="index", choices=["index", "write_keys", "recall"])
     ap.add_argument("--layers", type=int, default=3, help="recall: target layers")
     ap.add_argument("--threshold", type=float, default=0.5, help="recall: keep threshold")
@@ -639,9 +739,11 @@ def main():
     ap.add_argument("--recent", type=int, default=512, help="recall: recency-tail chunks")
     args = ap.parse_args()
     if args.op == "write_keys":
-        return run_write_keys(args)
+        run_write_keys(args)
+        return 0
     if args.op == "recall":
-        return run_recall(args)
+        run_recall(args)
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_native(args)
