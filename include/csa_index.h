@@ -56,7 +56,7 @@ extern "C" {
 /* Raised whenever an entry point, a struct layout or the meaning of an argument changes.
  * 2: csa_index_logits, csa_index_write_keys and the Level-1 recall entry points; 128 heads
  *    in the score and logit modes; a larger fused-path workspace (num_q + 2 row offsets). */
-#define CSA_ABI_VERSION 2
+#define CSA_ABI_VERSION 3
 
 #define CSA_HEAD_DIM 128        /* D: e4m3 bytes per record                         */
 #define CSA_NUM_HEADS 64        /* H of the Level-2 indexer                         */
@@ -194,6 +194,31 @@ csa_status csa_index_logits(const csa_index_args* args, float* logits, int64_t s
 csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_index_args* args,
                           int32_t k, int32_t* idx, float* vals, void* ws, size_t ws_bytes,
                           void* stream);
+
+/*
+ * Exact top-k of each row from G top-k lists of that row, for context-parallel
+ * scoring: one request's pages split across G GPUs, each scoring its own pages
+ * ("Two-level recall algorithm", Level 2, the top-512 over the scored history)
+ * and the G local lists gathered to one device. The global top-k of a row is
+ * contained in the union of its local top-k lists when every k_in >= k, so the
+ * merge is exact. Entries are ranked by (value desc, position asc): pass logits
+ * to reproduce csa_index_score_topk_fused's order exactly, or its sigmoid
+ * scores (the same order except among records whose fp32 scores tie).
+ *
+ * idx      [G, num_q, k_in] int32 device memory: logical positions, -1 = padding
+ *          (skipped, as is a NaN value). Positions must be distinct across the G
+ *          lists of a row (the shards hold disjoint pages).
+ * vals     [G, num_q, k_in] fp32 device memory: each entry's logit or score.
+ * out_idx  [num_q, k] int32: positions by (value desc, position asc), -1 padded.
+ * out_vals [num_q, k] fp32: the matching input values unchanged (-0 becomes +0);
+ *          padding 0.0f.
+ * 1 <= k_in, k <= CSA_MAX_K; num_lists >= 1; any num_lists * k_in (long lists are
+ * merged in rounds). No workspace.
+ * Errors: CSA_ERR_INVALID_ARG (a size out of range, a null pointer with num_q > 0),
+ * CSA_ERR_ALIGNMENT (pointers not 4-byte aligned), CSA_ERR_CUDA.
+ */
+csa_status csa_index_merge_topk(const int32_t* idx, const float* vals, int32_t num_lists, int32_t num_q,
+                                int32_t k_in, int32_t k, int32_t* out_idx, float* out_vals, void* stream);
 
 /*
  * Fused score + top-k: the scores never leave the chip ("Two-level recall algorithm",

@@ -1384,6 +1384,71 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
   }
 }
 
+// ------------------------------------------------------------------ merge of top-k lists
+
+// Context-parallel scoring splits one request's pages across G GPUs; each
+// returns its rows' local top-k (position, value). The global top-k of a row is
+// contained in the union of the local ones (every record of the global top-k
+// ranks at least as high in its own shard), so merging the G lists is exact.
+struct MergeListArgs {
+  const int32_t* idx;  // [G, num_q, k_in]
+  const float* vals;   // [G, num_q, k_in]
+  int32_t* out_idx;    // [num_q, k]
+  float* out_vals;     // [num_q, k]
+  int32_t num_lists, num_q, k_in, k;
+};
+
+// One CTA per row: the lists' valid entries (position >= 0, value not NaN)
+// become keys (value desc, position asc) appended to the candidate buffer; the
+// buffer is cut back to between k and merge_window(k) keys whenever the next
+// list might not fit, then sorted, and the first k written with their values
+// unchanged, padded with -1 / 0.
+__global__ void __launch_bounds__(kMergeThreads) merge_lists_kernel(const MergeListArgs A) {
+  extern __shared__ uint8_t smem_raw[];
+  MergeSmem& S = *reinterpret_cast<MergeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x;
+  const int32_t b = blockIdx.x;
+  const int window = merge_window(A.k);
+  if (tid == 0) {
+    S.sel.n = 0;
+    S.sel.tau = 0;
+  }
+  __syncthreads();
+  for (int g = 0; g < A.num_lists; ++g) {
+    if (static_cast<int>(S.sel.n) + A.k_in > kMergeCap)  // uniform: read after a barrier
+      shrink_if_above_reg<kMergeThreads, kMergeCap / kMergeThreads>(S.cand, S.scratch, kMergeCap - A.k_in, A.k,
+                                                                    window, &S.sel, 0, tid);
+    const int64_t base = (static_cast<int64_t>(g) * A.num_q + b) * A.k_in;
+    for (int j0 = 0; j0 < A.k_in; j0 += kMergeThreads) {  // whole warps in every round
+      const int j = j0 + tid;
+      int32_t pos = -1;
+      float v = 0.0f;
+      if (j < A.k_in) {
+        pos = A.idx[base + j];
+        v = A.vals[base + j];
+      }
+      const bool take = pos >= 0 && !isnan(v);
+      append_key(S.cand, take ? make_key(v, pos) : 0ull, take, &S.sel);
+    }
+    __syncthreads();
+  }
+  shrink_if_above_reg<kMergeThreads, kMergeCap / kMergeThreads>(S.cand, S.scratch, window, A.k, window, &S.sel, 0,
+                                                                tid);
+  const int n = static_cast<int>(S.sel.n);
+  sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
+  for (int j = tid; j < A.k; j += kMergeThreads) {
+    const int64_t o = static_cast<int64_t>(b) * A.k + j;
+    if (j < n) {
+      const uint64_t key = S.cand[j];
+      A.out_idx[o] = key_position(key);
+      A.out_vals[o] = key_value(key);
+    } else {
+      A.out_idx[o] = -1;
+      A.out_vals[o] = 0.0f;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ unfused top-k
 
 constexpr int kTopkThreads = 128;
@@ -1551,6 +1616,8 @@ csa_status device_setup(int* sms) {
         cudaFuncSetAttribute(merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(MergeSmem) + 16)) != cudaSuccess ||
         cudaFuncSetAttribute(merge_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(MergeSmem) + 16)) != cudaSuccess ||
+        cudaFuncSetAttribute(merge_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(MergeSmem) + 16)) != cudaSuccess ||
         cudaFuncSetAttribute(topk_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(TopkSmem) + 16)) != cudaSuccess)
@@ -1735,6 +1802,22 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
   if ((st = launch_w64(P, true, sms, s)) != CSA_OK) return st;
   if (event && cudaEventRecord(static_cast<cudaEvent_t>(event), s) != cudaSuccess) return CSA_ERR_CUDA;
   return launch_merge<true>(P, args->num_q, idx, vals, s, event == nullptr);
+}
+
+csa_status csa_index_merge_topk(const int32_t* idx, const float* vals, int32_t num_lists, int32_t num_q,
+                                int32_t k_in, int32_t k, int32_t* out_idx, float* out_vals, void* stream) {
+  if (num_lists < 1 || num_q < 0 || k_in < 1 || k_in > CSA_MAX_K || k < 1 || k > CSA_MAX_K)
+    return CSA_ERR_INVALID_ARG;
+  if (num_q == 0) return CSA_OK;
+  if (!idx || !vals || !out_idx || !out_vals) return CSA_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || !aligned(vals, 4) || !aligned(out_idx, 4) || !aligned(out_vals, 4))
+    return CSA_ERR_ALIGNMENT;
+  int sms = 0;
+  csa_status st = device_setup(&sms);
+  if (st != CSA_OK) return st;
+  MergeListArgs A{idx, vals, out_idx, out_vals, num_lists, num_q, k_in, k};
+  merge_lists_kernel<<<num_q, kMergeThreads, sizeof(MergeSmem) + 16, static_cast<cudaStream_t>(stream)>>>(A);
+  return launch_status();
 }
 
 csa_status csa_index_topk(const float* scores, int64_t score_stride, const csa_index_args* args, int32_t k,

@@ -97,6 +97,8 @@ def load(path: Optional[str] = None):
             lib.csa_recall_workspace_bytes.restype = sz
             lib.csa_recall_level1.argtypes = [ctypes.POINTER(RecallArgs), vp, sz, vp]
             lib.csa_recall_level1.restype = ctypes.c_int
+            lib.csa_index_merge_topk.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+            lib.csa_index_merge_topk.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -320,6 +322,24 @@ def csa_index_write_keys(keys: torch.Tensor, row_pos: torch.Tensor, kv: torch.Te
                   int(kv.shape[0]), int(kv.shape[1]), pt.data_ptr(), int(pt.shape[0]), int(pt.shape[1]),
                   _ptr(dev_status))
     _check(load().csa_index_write_keys(ctypes.byref(a), _stream(stream)), "csa_index_write_keys")
+
+
+def csa_index_merge_topk(idx: torch.Tensor, vals: torch.Tensor, k: int, out_idx: Optional[torch.Tensor] = None,
+                         out_vals: Optional[torch.Tensor] = None, stream=None):
+    """Exact top-k per row from G gathered top-k lists: idx int32 and vals fp32,
+    both [G, num_q, k_in] on the device. Returns (out_idx [num_q, k], out_vals)."""
+    if idx.dim() != 3 or vals.shape != idx.shape or idx.dtype != torch.int32 or vals.dtype != torch.float32:
+        raise ValueError("idx int32 and vals fp32 of one shape [G, num_q, k_in]")
+    idx, vals = idx.contiguous(), vals.contiguous()
+    g, nq, k_in = idx.shape
+    if out_idx is None:
+        out_idx = torch.empty((nq, k), dtype=torch.int32, device=idx.device)
+    if out_vals is None:
+        out_vals = torch.empty((nq, k), dtype=torch.float32, device=idx.device)
+    _check(load().csa_index_merge_topk(idx.data_ptr(), vals.data_ptr(), int(g), int(nq), int(k_in), int(k),
+                                       out_idx.data_ptr(), out_vals.data_ptr(), _stream(stream)),
+           "csa_index_merge_topk")
+    return out_idx, out_vals
 
 
 def csa_index_logits(problem: "Problem", logits: Optional[torch.Tensor] = None, stride=None, stream=None):

@@ -53,7 +53,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 
 def test_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 2
+    assert lib.csa_index_abi_version() == 3
     for s in range(6):
         assert native.status_str(s)
     assert native.status_str(99) == "unknown status"
@@ -110,6 +110,22 @@ def test_topk_rejects_bad_args(lib):
     assert t(0x5000, 128, ctypes.byref(a), 512, 0x1000, 0x2000, 0x3000, ws, None) == 1  # stride < 64*pt_stride
     assert t(None, 256, ctypes.byref(a), 512, 0x1000, 0x2000, 0x3000, ws, None) == 1
     assert lib.csa_index_score(None, 0x1000, 256, None) == 1
+
+
+def test_merge_topk_validates_on_the_host(lib):
+    f = lib.csa_index_merge_topk
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    ok = (0x1000, 0x2000)
+    assert f(*ok, 0, 4, 512, 512, 0x3000, 0x4000, None) == 1      # no lists
+    assert f(*ok, 2, -1, 512, 512, 0x3000, 0x4000, None) == 1     # negative rows
+    assert f(*ok, 2, 4, 0, 512, 0x3000, 0x4000, None) == 1        # k_in = 0
+    assert f(*ok, 2, 4, 1025, 512, 0x3000, 0x4000, None) == 1     # k_in > CSA_MAX_K
+    assert f(*ok, 2, 4, 512, 1025, 0x3000, 0x4000, None) == 1     # k > CSA_MAX_K
+    assert f(None, 0x2000, 2, 4, 512, 512, 0x3000, 0x4000, None) == 1
+    assert f(*ok, 2, 4, 512, 512, 0x3002, 0x4000, None) == 3      # misaligned output
+    assert f(*ok, 2, 0, 512, 512, None, None, None) == 0          # no rows: nothing to do
 
 
 def test_static_scratch_variant_validates_on_the_host(lib):
