@@ -89,7 +89,8 @@ def algorithmic_bytes(w) -> int:
     vis = w.visible_counts()
     pages = (vis + 63) // 64
     per_entry = 8 if w.resident is not None else 4
-    return int((vis * 132).sum() + (pages * per_entry).sum()
+    rec = 68 if getattr(w, "record_format", "e4m3") == "mxfp4" else 132
+    return int((vis * rec).sum() + (pages * per_entry).sum()
                + w.num_q * (64 * 128 * 2 + 64 * 4 + 4 + K_TOP * 8))
 
 
@@ -329,6 +330,8 @@ def run_native(args):
     build.build()
     native.load()
     w = synth.config(args.workload, seed=rank)
+    if args.op == "fp4":  # the same rows and pages over an MXFP4 cache (68-byte records)
+        w = synth.mxfp4_cache(w, seed=rank)
     prob = native.Problem.from_workload(w, device=dev)
     k = K_TOP
     ws = native.alloc_workspace(prob, k, dev)
@@ -468,19 +471,22 @@ def run_native(args):
 
     peak, peak_src = measured_peaks()
     achieved = alg_bytes / (phase1_ms / 1e3) / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic() if args.op == "index" else None
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.op == "index" else METRIC + ", MXFP4 records", "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": args.workload, "queries": w.num_q, "k": k, "records_per_step": keys,
+        "vs_baseline": None, "dtype": "e4m3" if args.op == "index" else "e2m1 (MXFP4) -> e4m3", "data": "synthetic",
+        "config": {"workload": args.workload, "record_format": getattr(w, "record_format", "e4m3"),
+                   "queries": w.num_q, "k": k, "records_per_step": keys,
                    "records_per_query": "65536..131072" if args.workload == "long_ragged_decode" else None,
                    "key_bytes_per_step": w.k_bytes(), "algorithmic_bytes_per_step": alg_bytes,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
                    "seed": rank},
         "queries_per_s": w.num_q * world / (ms_max / 1e3),
         "gbs": alg_bytes * world / (ms_max / 1e3) / 1e9,
-        "roofline": {"kernel": "w64::score_kernel_w64<topk> (scoring phase)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": ("w64::score_kernel_w64<topk, e4m3> (scoring phase)" if args.op == "index" else
+                                "w64::score_kernel_w64<topk, mxfp4> (scoring phase)"), "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "phase1_ms": phase1_ms,
                      "algorithmic_bytes_per_launch": alg_bytes},
@@ -503,7 +509,7 @@ def run_native(args):
             "full_history_scoring": indexer_gflop(21, 262144),
             "resident_scoring_and_level1": indexer_gflop(21, 384 * 64) + indexer_gflop(3, 262144, heads=128) / 64},
     }
-    if rank == 0 and world == 1 and not args.no_per_config:
+    if rank == 0 and world == 1 and not args.no_per_config and args.op == "index":
         line["per_config"] = measure_configs(PER_CONFIG, dev)
         # the next-row kernels on the same workload's geometry (their own lines:
         # bench.py --op write_keys / --op recall)
@@ -732,7 +738,8 @@ def main():
     ap.add_argument("--workload", default="long_ragged_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the other configs' measurements")
-    ap.add_argument("--op", default="index", choices=["index", "write_keys", "recall"])
+    ap.add_argument("--op", default="index", choices=["index", "fp4", "write_keys", "recall"],
+                    help="index: the indexer on e4m3 records (headline); fp4: the same on MXFP4 records")
     ap.add_argument("--layers", type=int, default=3, help="recall: target layers")
     ap.add_argument("--threshold", type=float, default=0.5, help="recall: keep threshold")
     ap.add_argument("--sink", type=int, default=4, help="recall: attention-sink chunks")

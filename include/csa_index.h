@@ -56,7 +56,7 @@ extern "C" {
 /* Raised whenever an entry point, a struct layout or the meaning of an argument changes.
  * 2: csa_index_logits, csa_index_write_keys and the Level-1 recall entry points; 128 heads
  *    in the score and logit modes; a larger fused-path workspace (num_q + 2 row offsets). */
-#define CSA_ABI_VERSION 3
+#define CSA_ABI_VERSION 4
 
 #define CSA_HEAD_DIM 128        /* D: e4m3 bytes per record                         */
 #define CSA_NUM_HEADS 64        /* H of the Level-2 indexer                         */
@@ -80,7 +80,7 @@ typedef enum csa_status {
 enum {
   CSA_DEV_PAGE_OOB = 1,      /* page_table entry outside [0, num_pages): page skipped      */
   CSA_DEV_RESIDENT_OOB = 2,  /* resident page id outside [0, ceil(len/64)): page skipped  */
-  CSA_DEV_RANGE = 4,         /* q holds a non-finite value                                 */
+  CSA_DEV_RANGE = 4,         /* q holds a non-finite value; or an MXFP4 input outside the exact range */
   CSA_DEV_TIMEOUT = 8,       /* an on-chip pipeline wait ran past its limit; output invalid */
   CSA_DEV_BAD_REQUEST = 16,  /* q_req entry outside [0, num_req): query treated as empty   */
   CSA_DEV_LEN_OOB = 32       /* q_len < 0, q_len > 64*pt_stride, or n_resident outside
@@ -119,6 +119,32 @@ enum {
  * rows average at least 16 tiles, kept as 32-bit offsets: that total must stay below
  * 2^31 (about 5 * 10^11 records scored per call).
  */
+/*
+ * Record formats of the compressed-K cache (csa_index_args.record_format):
+ *
+ * CSA_RECORD_E4M3  132-byte records: head_dim e4m3 bytes then a little-endian fp32
+ *                  scale (FlashMemory-DeepSeek-V4, "compressed_k format"); 64 records
+ *                  a page, page_stride_bytes >= 8448.
+ * CSA_RECORD_MXFP4 68-byte records (the published model FP4-rounds the index key and
+ *                  query alike: the BatchGen #153 commit log's indexer quantisation
+ *                  notes and "DeepSeek-V4.1 native paged runtime"; the pages print no
+ *                  block size or layout, so the OCP MXFP4 reading is taken): 64 bytes of
+ *                  e2m1 codes, element 2j in the low nibble of byte j, then the 4 UE8M0
+ *                  scale bytes of the record's 32-element blocks (2^(byte - 127); 255 is
+ *                  NaN). 64 records a page, page_stride_bytes >= 4352. The query is
+ *                  MXFP4-rounded per head the same way (scale 2^(floor(log2 amax) - 2),
+ *                  nearest e2m1 value, ties to even, saturating at 6) before the score,
+ *                  which is the indexer's on the dequantised values. 64 heads only
+ *                  (csa_index_score, csa_index_logits and the fused entry points; the
+ *                  unfused csa_index_topk reads no keys). A record holding a NaN scale
+ *                  byte is left out (CSA_DEV_RANGE). The kernel scores exactly when the
+ *                  block exponents of a record, or of one query head, span at most 14;
+ *                  a wider span is still scored, its smallest blocks rounded, and flagged
+ *                  CSA_DEV_RANGE.
+ */
+#define CSA_RECORD_E4M3 0
+#define CSA_RECORD_MXFP4 1
+
 typedef struct csa_index_args {
   const void* q;
   const float* fused_w;
@@ -137,7 +163,7 @@ typedef struct csa_index_args {
   const int32_t* resident;
   const int32_t* n_resident;
   int32_t res_stride;
-  int32_t reserved1;         /* must be 0 */
+  int32_t record_format;     /* CSA_RECORD_E4M3 (0) or CSA_RECORD_MXFP4 (1); see below */
   int32_t* dev_status;
 } csa_index_args;
 

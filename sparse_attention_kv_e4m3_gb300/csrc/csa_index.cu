@@ -56,6 +56,8 @@ constexpr int kD = 128;
 constexpr int kPage = 64;
 constexpr int kRec = 132;
 constexpr int kPageBytes = kPage * kRec;  // 8448
+constexpr int kFp4Rec = 68;                // MXFP4 record: 64 code bytes + 4 UE8M0 block scales
+constexpr int kFp4PageBytes = kPage * kFp4Rec;  // 4352
 constexpr int kMmaRows = 128;             // records per MMA (M)
 constexpr int kSub = 2;                   // MMA sub-tiles per tile
 constexpr int kTile = kSub * kMmaRows;    // records per tile: the unit of every hand-off
@@ -154,6 +156,7 @@ struct Params {
   int32_t res_stride;
   int32_t k;
   int32_t grid;         // CTAs of the phase-1 kernel (slot numbering)
+  int32_t fmt;          // record format: CSA_RECORD_E4M3 or CSA_RECORD_MXFP4
   int32_t raw_logits;   // score mode: write the logit instead of its sigmoid
   int32_t fold;         // score mode: 0 store, CSA_FOLD_MAX / CSA_FOLD_ADD fold the score into the output
 };
@@ -1568,7 +1571,8 @@ enum { kNeedQ = 1, kNeedKv = 2, kAllowWide = 4 };  // kAllowWide: 128 heads acce
 
 csa_status check_args(const csa_index_args* a, int need) {
   if (!a) return CSA_ERR_INVALID_ARG;
-  if (a->reserved0 != 0 || a->reserved1 != 0) return CSA_ERR_INVALID_ARG;
+  if (a->reserved0 != 0) return CSA_ERR_INVALID_ARG;
+  if (a->record_format != CSA_RECORD_E4M3 && a->record_format != CSA_RECORD_MXFP4) return CSA_ERR_INVALID_ARG;
   if (a->num_q < 0 || a->num_req < 0 || a->pt_stride < 0 || a->res_stride < 0) return CSA_ERR_INVALID_ARG;
   if (a->num_q == 0) return CSA_OK;
   if (!a->q_len) return CSA_ERR_INVALID_ARG;
@@ -1582,6 +1586,7 @@ csa_status check_args(const csa_index_args* a, int need) {
   if (need & kNeedQ) {
     if (a->head_dim != kD || !(a->num_heads == kH || ((need & kAllowWide) && a->num_heads == 2 * kH)))
       return CSA_ERR_UNSUPPORTED;
+    if (a->record_format == CSA_RECORD_MXFP4 && a->num_heads != kH) return CSA_ERR_UNSUPPORTED;
     if (!a->q || !a->fused_w) return CSA_ERR_INVALID_ARG;
     if (!aligned(a->q, 16) || !aligned(a->fused_w, 4)) return CSA_ERR_ALIGNMENT;
   }
@@ -1589,7 +1594,8 @@ csa_status check_args(const csa_index_args* a, int need) {
     if (!a->kv || !a->page_table || a->num_pages < 1 || a->pt_stride < 1 || a->num_req < 1)
       return CSA_ERR_INVALID_ARG;
     if (a->num_pages > INT32_MAX) return CSA_ERR_INVALID_ARG;
-    if (a->page_stride_bytes < kPageBytes) return CSA_ERR_INVALID_ARG;
+    if (a->page_stride_bytes < (a->record_format == CSA_RECORD_MXFP4 ? kFp4PageBytes : kPageBytes))
+      return CSA_ERR_INVALID_ARG;
     if (a->page_stride_bytes % 16 != 0 || !aligned(a->kv, 16)) return CSA_ERR_ALIGNMENT;
     if (!aligned(a->page_table, 4)) return CSA_ERR_ALIGNMENT;
   } else if (a->page_table && !aligned(a->page_table, 4)) {
@@ -1607,9 +1613,15 @@ csa_status device_setup(int* sms) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return CSA_ERR_CUDA;
     if (n * kTopkCtasPerSm > CSA_MAX_CTAS) return CSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(w64::score_kernel_w64<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(w64::score_kernel_w64<false, CSA_RECORD_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(w64::score_kernel_w64<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(w64::score_kernel_w64<true, CSA_RECORD_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(w64::score_kernel_w64<false, CSA_RECORD_MXFP4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(w64::score_kernel_w64<true, CSA_RECORD_MXFP4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(score_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes<128>)) != cudaSuccess ||
@@ -1647,6 +1659,7 @@ Params params_of(const csa_index_args* a) {
   P.num_req = a->num_req;
   P.pt_stride = a->pt_stride;
   P.res_stride = a->res_stride;
+  P.fmt = a->record_format;
   return P;
 }
 
@@ -1660,10 +1673,15 @@ csa_status launch_status() { return cudaGetLastError() == cudaSuccess ? CSA_OK :
 
 // The 64-head scorer in score / logit mode or top-k mode.
 csa_status launch_w64(const Params& P, bool topk, int sms, cudaStream_t s) {
-  if (topk)
-    w64::score_kernel_w64<true><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
+  const bool fp4 = P.fmt == CSA_RECORD_MXFP4;
+  if (topk && fp4)
+    w64::score_kernel_w64<true, CSA_RECORD_MXFP4><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
+  else if (topk)
+    w64::score_kernel_w64<true, CSA_RECORD_E4M3><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
+  else if (fp4)
+    w64::score_kernel_w64<false, CSA_RECORD_MXFP4><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
   else
-    w64::score_kernel_w64<false><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
+    w64::score_kernel_w64<false, CSA_RECORD_E4M3><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
   return launch_status();
 }
 

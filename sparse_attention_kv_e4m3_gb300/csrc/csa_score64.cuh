@@ -158,7 +158,9 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
 
 // Lanes 0..7 copy the 8 pages of each tile in lockstep, page j of tile t into
 // ring slot (8t + j) % kPages.
+template <int kFmt>
 __device__ void role_issuer(const Params& P, Smem& S) {
+  constexpr uint32_t kBytes = kFmt == CSA_RECORD_MXFP4 ? kFp4PageBytes : kPageBytes;  // a page's records
   const int lane = threadIdx.x & 31;
   const int64_t nt = S.plan.ntiles;
   const uint64_t policy = policy_evict_first();
@@ -184,8 +186,8 @@ __device__ void role_issuer(const Params& P, Smem& S) {
         S.info[s] = e;
         const uint32_t fb = smem_u32(&S.full[s]);
         if (e.nrows > 0) {
-          mbar_arrive_expect_tx(fb, kPageBytes);
-          bulk_g2s_hint(smem_u32(S.pages[s]), P.kv + static_cast<int64_t>(e.phys) * P.page_stride, kPageBytes, fb,
+          mbar_arrive_expect_tx(fb, kBytes);
+          bulk_g2s_hint(smem_u32(S.pages[s]), P.kv + static_cast<int64_t>(e.phys) * P.page_stride, kBytes, fb,
                         policy);
         } else {
           mbar_arrive(fb);
@@ -210,7 +212,9 @@ __device__ void role_issuer(const Params& P, Smem& S) {
 // One of the two issuing threads: class sub-tile c of every half-tile (classes
 // c and 2 + c of each tile). Both commit to the half-tile's accumulator-ready
 // barrier, to the query slot's release at a segment end and to the final drain.
+template <int kFmt>
 __device__ void role_mma(const Params& P, Smem& S, const int c) {
+  constexpr int kTerms = kFmt == CSA_RECORD_MXFP4 ? 1 : 2;  // an MXFP4 query is one e4m3 term
   CursorT<kTP> cur;
   cur.init(P, S.plan);
   const uint32_t tmem = S.tmem_base;
@@ -238,7 +242,7 @@ __device__ void role_mma(const Params& P, Smem& S, const int c) {
       tc_fence_after();
       const uint32_t d = tmem + d_col(ds) + kH * c, a = tmem + a_col(g) + 32 * c;
 #pragma unroll
-      for (int term = 0; term < 2; ++term)
+      for (int term = 0; term < kTerms; ++term)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_e4m3_ts(d, a + 8 * kk, bdesc[term][kk], kIdesc, (term | kk) != 0);
       mma_commit(smem_u32(&S.dfull[ds]));
@@ -296,9 +300,247 @@ __device__ __forceinline__ uint32_t stage_record(const uint8_t* row, int r, uint
   return scale;
 }
 
+// ------------------------------------------------------------------ MXFP4 records and queries
+//
+// An MXFP4 record (68 bytes: 64 bytes of e2m1 codes, element 2j in the low nibble
+// of byte j, then the UE8M0 scale bytes of its four 32-element blocks) is turned
+// into the 128 e4m3 bytes the MMA reads, exactly: with e_b the exponent of block
+// b and E the record's largest, element x = v * 2^e_b (v an e2m1 value) is
+// stored as the e4m3 value v * 2^(e_b - E + 6), and 2^(E - 6) becomes the
+// record's scale for the epilogue. v * 2^k is an e4m3 value for every e2m1 v
+// when -8 <= k <= 6 (the largest, 6 * 2^6 = 384, stays below 448; the smallest,
+// 0.5 * 2^-8 = 2^-9, is e4m3's smallest subnormal), i.e. whenever the record's
+// block exponents span at most 14. The query is MXFP4-rounded per head the same
+// way and converted relative to its head's largest block exponent, so a single
+// e4m3 term carries it exactly (no lo term: half the MMAs).
+
+// e4m3 codes of the 8 e2m1 magnitudes (0, 0.5, 1, 1.5, 2, 3, 4, 6), four per word.
+constexpr uint32_t kE2m1ToE4m3Lo = 0x3C383000u, kE2m1ToE4m3Hi = 0x4C484440u;
+
+// e2m1 magnitude code (0..7) of a >= 0 (a value already divided by its block
+// scale): round to nearest, ties to the even code, saturating at 6. Each
+// comparison is one of the midpoints 0.25, 0.75, ..., 5; a tie stays on the even
+// side (e.g. 0.75 goes up to 1.0 = code 2, 1.25 stays at 1.0).
+__device__ __forceinline__ uint32_t e2m1_mag(float a) {
+  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) + static_cast<uint32_t>(a > 1.25f) +
+         static_cast<uint32_t>(a >= 1.75f) + static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
+         static_cast<uint32_t>(a > 5.0f);
+}
+
+// Value of e2m1 magnitude code m: exponent m >> 1 (bias 1, 0 subnormal), mantissa m & 1.
+__device__ __forceinline__ float e2m1_value(uint32_t m) {
+  const int E = static_cast<int>(m >> 1);
+  const float mant = (m & 1u) ? 1.5f : 1.0f;
+  return E == 0 ? 0.5f * static_cast<float>(m & 1u) : mant * __int_as_float((E - 1 + 127) << 23);
+}
+
+// 2^k as an fp32 value for -149 <= k <= 127 (subnormal below -126).
+__device__ __forceinline__ float pow2f(int k) {
+  return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+// Two fp32 values as e4m3 codes (a in the low byte), round to nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// Block exponent of MXFP4: floor(log2 amax) - 2, clamped to [-127, 127]; -127
+// for a block of zeros.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int E2;
+  (void)frexpf(amax, &E2);  // amax = f * 2^E2, f in [0.5, 1)
+  const int e = E2 - 3;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// The 8 e4m3 codes of the e2m1 magnitudes times 2^k (k <= 6), as (lo, hi) words
+// for a byte-permute lookup. For k >= -5 all eight are normal and the exponent
+// fields just move by k; below, each is converted (exact down to k = -8).
+__device__ __forceinline__ void e4m3_table(int k, uint32_t& lo, uint32_t& hi) {
+  if (k >= -5) {
+    const uint32_t add = static_cast<uint32_t>(k * 8);
+    lo = kE2m1ToE4m3Lo + add * 0x01010100u;  // code 0 stays 0
+    hi = kE2m1ToE4m3Hi + add * 0x01010101u;
+  } else {
+    const float f = pow2f(k < -40 ? -40 : k);
+    lo = e4m3x2(0.0f, 0.5f * f) | (e4m3x2(1.0f * f, 1.5f * f) << 16);
+    hi = e4m3x2(2.0f * f, 3.0f * f) | (e4m3x2(4.0f * f, 6.0f * f) << 16);
+  }
+}
+
+// PTX byte permute in its default mode: byte n of the result is byte (sel nibble n
+// & 7) of {b, a} (a bytes 0-3); bit 3 of the nibble replicates that byte's sign bit
+// over the whole result byte instead.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Four e2m1 codes (the nibbles of c16, element i in nibble i) as four e4m3 bytes
+// (element i in byte i) through the table (lo, hi): the magnitude by a byte-permute
+// lookup on the low three bits of each nibble, the sign from bit 3 (a permute of
+// 0x80 bytes in sign-replicate mode gives 0xFF for a set bit and 0x80 otherwise;
+// xor 0x80 and plus 1 per byte leave 0x80 or 0x01, no carry between bytes).
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t c16, uint32_t lo, uint32_t hi) {
+  const uint32_t mag = prmt(lo, hi, c16 & 0x7777u);
+  const uint32_t rep = prmt(0x80808080u, 0x80808080u, c16 & 0xFFFFu);
+  return mag | (((rep ^ 0x80808080u) + 0x01010101u) & 0x80808080u);
+}
+
+// Words r .. r + 15 of the 20 loaded (the record's code bytes) into c; word
+// r + 16 (its four scale bytes) into sb.
+template <int R>
+__device__ __forceinline__ void pick_record_fp4(const uint32_t (&w)[20], uint32_t (&c)[16], uint32_t& sb) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) c[j] = w[R + j];
+  sb = w[R + 16];
+}
+
+// Stages this lane's MXFP4 record of class r (run-time, warp-uniform: the same
+// reason as stage_record) from the 16-byte-aligned group row `row` (272 bytes =
+// 4 records) into TMEM column address ta as 128 e4m3 bytes; returns the record's
+// scale bits 2^(E - 6), NaN bits for a record holding a NaN scale byte. A block
+// span above 14 is flagged (CSA_DEV_RANGE) and scored with its smallest blocks
+// rounded.
+__device__ __forceinline__ uint32_t stage_record_fp4(const uint8_t* row, int r, uint32_t ta, int32_t* flags) {
+  uint32_t w[20];
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    const uint4 q4 = *reinterpret_cast<const uint4*>(row + 64 * r + 16 * j);
+    w[4 * j] = q4.x;
+    w[4 * j + 1] = q4.y;
+    w[4 * j + 2] = q4.z;
+    w[4 * j + 3] = q4.w;
+  }
+  uint32_t c[16], sb;
+  switch (r) {
+    case 0: pick_record_fp4<0>(w, c, sb); break;
+    case 1: pick_record_fp4<1>(w, c, sb); break;
+    case 2: pick_record_fp4<2>(w, c, sb); break;
+    default: pick_record_fp4<3>(w, c, sb); break;
+  }
+  int e[4], emax = -127;
+  bool nan_scale = false;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int byte = static_cast<int>((sb >> (8 * b)) & 0xFFu);
+    nan_scale |= byte == 255;
+    e[b] = byte - 127;
+    emax = max(emax, e[b]);
+  }
+  uint32_t v[32];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int k = e[b] - emax + 6;
+    if (k < -8) *flags |= CSA_DEV_RANGE;
+    uint32_t lo, hi;
+    e4m3_table(k, lo, hi);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t cw = c[4 * b + j];
+      v[8 * b + 2 * j] = e2m1x4_to_e4m3(cw & 0xFFFFu, lo, hi);
+      v[8 * b + 2 * j + 1] = e2m1x4_to_e4m3(cw >> 16, lo, hi);
+    }
+  }
+  tmem_st32(ta, v);
+  if (nan_scale) {
+    *flags |= CSA_DEV_RANGE;
+    return kNaNBits;
+  }
+  return __float_as_uint(pow2f(emax - 6));
+}
+
+// MXFP4 rounding of 4 elements of one head (x[0..3], its block's exponent e_b,
+// its head's largest E) as one word of e4m3 codes of v * 2^(e_b - E + 6).
+__device__ __forceinline__ uint32_t fp4_query_word(const float (&x)[4], int eb, int E, int32_t* flags) {
+  const float inv = pow2f(-eb);                   // 1 / block scale (e_b in [-127, 127])
+  const int k = eb - E + 6;
+  if (k < -8) *flags |= CSA_DEV_RANGE;
+  const float f = pow2f(k < -40 ? -40 : k);
+  float y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float m = e2m1_value(e2m1_mag(fabsf(x[i]) * inv)) * f;
+    y[i] = signbit(x[i]) ? -m : m;
+  }
+  return e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
+}
+
+// Splits heads h0 .. h0 + 15 of query row b into query slot qs (one warp), MXFP4:
+// lane l holds elements 4l .. 4l + 3 of each head, so the 8 lanes of a block
+// reduce its amax and all 32 lanes the head's largest block exponent.
+__device__ void prep_query_part_fp4(const Params& P, Smem& S, int32_t b, int qs, int h0, int32_t* flags) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t* qrow = P.q + (static_cast<int64_t>(b) * kH + h0) * kD;
+  const float w_mine = lane < 16 ? __ldg(P.w + static_cast<int64_t>(b) * kH + h0 + lane) : 0.0f;
+  uint8_t* hi = S.qbuf[qs][0];
+  uint2 raw[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) raw[j] = __ldg(reinterpret_cast<const uint2*>(qrow + j * kD + lane * 4));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int h = h0 + j;
+    float x[4];
+    x[0] = __uint_as_float(raw[j].x << 16);
+    x[1] = __uint_as_float(raw[j].x & 0xFFFF0000u);
+    x[2] = __uint_as_float(raw[j].y << 16);
+    x[3] = __uint_as_float(raw[j].y & 0xFFFF0000u);
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));  // the block's 8 lanes
+    if (!isfinite(a)) *flags |= CSA_DEV_RANGE;
+    const int eb = mx_block_exp(isfinite(a) ? a : 0.0f);
+    int E = eb;
+#pragma unroll
+    for (int o = 16; o >= 8; o >>= 1) E = max(E, __shfl_xor_sync(0xFFFFFFFFu, E, o));
+    *reinterpret_cast<uint32_t*>(hi + qbuf_offset(h, lane >> 2) + (lane & 3) * 4) = fp4_query_word(x, eb, E, flags);
+    if (lane == j) S.wbuf[qs][h] = w_mine * pow2f(E - 6);
+  }
+}
+
+// The first segment's MXFP4 query by the whole CTA in the prologue (thread t:
+// the 16 elements 16p .. 16p + 15 of head t / 8, p = t % 8; a block is two
+// threads).
+__device__ void prep_first_query_fp4(const Params& P, Smem& S, int32_t b, int32_t* flags) {
+  const int tid = threadIdx.x, p = tid & 7, h = tid >> 3;
+  const uint16_t* src = P.q + (static_cast<int64_t>(b) * kH + h) * kD + p * 16;
+  const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(src + 8));
+  const float wv = p == 0 ? __ldg(P.w + static_cast<int64_t>(b) * kH + h) : 0.0f;
+  const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
+  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));  // the block's two threads
+  if (!isfinite(a)) *flags |= CSA_DEV_RANGE;
+  const int eb = mx_block_exp(isfinite(a) ? a : 0.0f);
+  int E = eb;
+#pragma unroll
+  for (int o = 4; o >= 2; o >>= 1) E = max(E, __shfl_xor_sync(0xFFFFFFFFu, E, o));  // the head's 8 threads
+  uint32_t wd[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float xi[4] = {x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]};
+    wd[i] = fp4_query_word(xi, eb, E, flags);
+  }
+  *reinterpret_cast<uint4*>(S.qbuf[0][0] + qbuf_offset(h, p)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  if (p == 0) S.wbuf[0][h] = wv * pow2f(E - 6);
+}
+
 // One warp of a worker group: group gi owns classes 2gi and 2gi + 1 of every tile.
-template <bool kTopk>
+template <bool kTopk, int kFmt>
 __device__ void role_worker(const Params& P, Smem& S) {
+  int32_t wflags = 0;  // CSA_DEV_RANGE from MXFP4 records
   const int e = (threadIdx.x >> 5) - kWarpWorker;  // 0..7
   const int gi = e >> 2;                            // worker group
   const int c0 = 2 * gi;                            // the group's first class
@@ -320,10 +562,20 @@ __device__ void role_worker(const Params& P, Smem& S) {
     const bool ok = mbar_wait(smem_u32(&S.full[s]), static_cast<uint32_t>((pg / kPages) & 1), &S.abort_flag);
     if (!__all_sync(0xFFFFFFFFu, ok)) return false;
     const PageInfo pi = S.info[s];
-    const uint8_t* row = S.pages[s] + grp * kGroupBytes;
     const uint32_t ta = tmem + a_col(gi) + lane_off;
-    sc[0] = stage_record(row, c0, ta);
-    sc[1] = stage_record(row, c0 + 1, ta + 32);
+    if constexpr (kFmt == CSA_RECORD_MXFP4) {
+      // a slot's records past the page's visible rows (or a slot never filled) hold
+      // whatever bytes were there: only visible records raise flags
+      const uint8_t* row = S.pages[s] + grp * (4 * kFp4Rec);
+      int32_t f0 = 0, f1 = 0;
+      sc[0] = stage_record_fp4(row, c0, ta, &f0);
+      sc[1] = stage_record_fp4(row, c0 + 1, ta + 32, &f1);
+      wflags |= (4 * grp + c0 < pi.nrows ? f0 : 0) | (4 * grp + c0 + 1 < pi.nrows ? f1 : 0);
+    } else {
+      const uint8_t* row = S.pages[s] + grp * kGroupBytes;
+      sc[0] = stage_record(row, c0, ta);
+      sc[1] = stage_record(row, c0 + 1, ta + 32);
+    }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -447,6 +699,10 @@ __device__ void role_worker(const Params& P, Smem& S) {
     }
     cur.advance(P);
   }
+  if constexpr (kFmt == CSA_RECORD_MXFP4) {
+    wflags = __reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(wflags));
+    if (lane == 0 && wflags) atomicOr(&S.status, wflags);
+  }
 }
 
 // ------------------------------------------------------------------ selector
@@ -495,6 +751,7 @@ __device__ void prep_query_part(const Params& P, Smem& S, int32_t b, int qs, int
 // (16 regions, one per class and worker warp) enter a shared buffer, which is
 // cut back to between k and loose_keep(k) keys when it could overflow; each
 // segment's survivors go to workspace slot (row + CTA).
+template <int kFmt>
 __device__ void role_select(const Params& P, Smem& S) {
   const int g = threadIdx.x - kWarpSelect * 32;
   const int sw = g >> 5, lane = g & 31;
@@ -510,7 +767,10 @@ __device__ void role_select(const Params& P, Smem& S) {
   auto prep_next = [&]() {
     if (prep_done >= S.plan.ntiles) return;  // uniform
     const int qs = prep_seg & 1;
-    prep_query_part(P, S, prep_b, qs, 16 * sw, &qflags);
+    if constexpr (kFmt == CSA_RECORD_MXFP4)
+      prep_query_part_fp4(P, S, prep_b, qs, 16 * sw, &qflags);
+    else
+      prep_query_part(P, S, prep_b, qs, 16 * sw, &qflags);
     fence_proxy_async_smem();  // the MMA reads the query through the async proxy
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.qfull[qs]));
@@ -592,9 +852,33 @@ __device__ void role_select(const Params& P, Smem& S) {
   if (qflags) atomicOr(&S.status, qflags);
 }
 
+// Score mode, MXFP4: warp 12 splits the CTA's later queries (as prep_segments
+// does for e4m3 records), 16 heads at a time.
+__device__ void prep_segments_fp4(const Params& P, Smem& S) {
+  const int lane = threadIdx.x & 31;
+  int32_t flags = 0;
+  int64_t done = query_tiles<kTP>(P, S.plan.b0) - S.plan.lt0;
+  int32_t b = next_nonempty<kTP>(P, S.plan.b0 + 1);
+  for (int seg = 1; done < S.plan.ntiles; ++seg) {
+    const int qs = seg & 1;
+    int ok = 1;
+    if (lane == 0)
+      ok = mbar_wait(smem_u32(&S.qempty[qs]), static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), &S.abort_flag);
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+    for (int h0 = 0; h0 < kH; h0 += 16) prep_query_part_fp4(P, S, b, qs, h0, &flags);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.qfull[qs]));
+    done += query_tiles<kTP>(P, b);
+    b = next_nonempty<kTP>(P, b + 1);
+  }
+  flags = static_cast<int32_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(flags)));
+  if (lane == 0 && flags) atomicOr(&S.status, flags);
+}
+
 // ------------------------------------------------------------------ kernel
 
-template <bool kTopk>
+template <bool kTopk, int kFmt>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = smem_of(smem_raw);
@@ -644,7 +928,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
   }
   {
     int32_t qflags = 0;
-    prep_first_query<kH>(P, S, S.plan.b0, &qflags);
+    if constexpr (kFmt == CSA_RECORD_MXFP4)
+      prep_first_query_fp4(P, S, S.plan.b0, &qflags);
+    else
+      prep_first_query<kH>(P, S, S.plan.b0, &qflags);
     fence_proxy_async_smem();  // the MMA reads the query through the async proxy
     if (qflags) atomicOr(&S.status, qflags);
   }
@@ -654,19 +941,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
   if (tid == 0) mbar_arrive(smem_u32(&S.qfull[0]));
 
   if (warp == kWarpIssuer) {
-    role_issuer(P, S);
+    role_issuer<kFmt>(P, S);
   } else if (warp == kWarpMma) {
-    if ((tid & 31) == 0) role_mma(P, S, 0);
+    if ((tid & 31) == 0) role_mma<kFmt>(P, S, 0);
   } else if (warp == kWarpMma2) {
-    if ((tid & 31) == 0) role_mma(P, S, 1);
+    if ((tid & 31) == 0) role_mma<kFmt>(P, S, 1);
   } else if (warp == kWarpWalker) {
     walk_pages<kTP>(P, S);
   } else if (warp < kWarpSelect) {
-    role_worker<kTopk>(P, S);
+    role_worker<kTopk, kFmt>(P, S);
   } else if (kTopk) {
-    role_select(P, S);
+    role_select<kFmt>(P, S);
   } else if (warp == kWarpSelect) {
-    prep_segments<kH, kTP>(P, S);
+    if constexpr (kFmt == CSA_RECORD_MXFP4)
+      prep_segments_fp4(P, S);
+    else
+      prep_segments<kH, kTP>(P, S);
   }
 
   tc_fence_before();

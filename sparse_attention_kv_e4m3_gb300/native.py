@@ -51,7 +51,7 @@ class Args(ctypes.Structure):
         ("resident", ctypes.c_void_p),
         ("n_resident", ctypes.c_void_p),
         ("res_stride", ctypes.c_int32),
-        ("reserved1", ctypes.c_int32),
+        ("record_format", ctypes.c_int32),
         ("dev_status", ctypes.c_void_p),
     ]
 
@@ -104,6 +104,7 @@ def load(path: Optional[str] = None):
 
 
 KEYS_F32, KEYS_BF16 = 0, 1
+RECORD_E4M3, RECORD_MXFP4 = 0, 1
 
 
 class WriteArgs(ctypes.Structure):
@@ -184,6 +185,7 @@ class Problem:
     n_resident: Optional[torch.Tensor] = None
     dev_status: Optional[torch.Tensor] = None
     num_req: Optional[int] = None
+    record_format: int = 0  # RECORD_E4M3 or RECORD_MXFP4
 
     def args(self) -> Args:
         a = Args()
@@ -210,6 +212,7 @@ class Problem:
         if self.resident is not None:
             a.res_stride = int(self.resident.stride(0))
         a.dev_status = _ptr(self.dev_status)
+        a.record_format = int(self.record_format)
         return a
 
     @property
@@ -232,7 +235,8 @@ class Problem:
         return Problem(
             q=q, fused_w=t(w.fused_w), kv=t(w.kv), page_table=t(w.page_table), q_len=t(w.q_len),
             q_req=t(w.q_req), resident=t(w.resident), n_resident=t(w.n_resident),
-            dev_status=torch.zeros(1, dtype=torch.int32, device=device) if dev_status else None)
+            dev_status=torch.zeros(1, dtype=torch.int32, device=device) if dev_status else None,
+            record_format=RECORD_MXFP4 if getattr(w, "record_format", "e4m3") == "mxfp4" else RECORD_E4M3)
 
 
 def workspace_bytes(problem_or_args, k: int) -> int:

@@ -53,7 +53,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 
 def test_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 3
+    assert lib.csa_index_abi_version() == 4
     for s in range(6):
         assert native.status_str(s)
     assert native.status_str(99) == "unknown status"
@@ -87,7 +87,7 @@ def _fake_args(**kw):
 @pytest.mark.parametrize("change,want", [
     (dict(head_dim=64), 2), (dict(num_heads=96), 2), (dict(num_heads=256), 2), (dict(q=0), 1), (dict(q=0x10008), 3),
     (dict(kv=0x30004), 3), (dict(page_stride_bytes=8440), 1), (dict(page_stride_bytes=8456), 3),
-    (dict(num_q=-1), 1), (dict(reserved0=1), 1), (dict(q_len=0), 1), (dict(num_req=2), 1),
+    (dict(num_q=-1), 1), (dict(reserved0=1), 1), (dict(record_format=2), 1), (dict(q_len=0), 1), (dict(num_req=2), 1),
     (dict(resident=0x60000), 1), (dict(num_pages=0), 1), (dict(page_table=0x40002), 3),
 ])
 def test_score_rejects_bad_args(lib, change, want):
