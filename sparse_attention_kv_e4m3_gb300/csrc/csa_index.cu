@@ -1272,12 +1272,24 @@ constexpr int kMergeCap = 4096;   // candidate buffer; a row with more is cut ba
 constexpr int kMergeSlots = CSA_MAX_CTAS + 1;
 static_assert(2 * CSA_MAX_K <= kMergeCap, "after a cut to merge_window(k), any slot must fit");
 
+constexpr int kRankBins = 1024;  // bins of the final rank sort
+static_assert(kMergeThreads / 32 <= 8, "the rank sort's per-warp partials fit sel.part");
+
 struct MergeSmem {
   uint64_t cand[kMergeCap];
-  uint64_t scratch[CSA_MAX_K];
+  uint64_t scratch[CSA_MAX_K];  // also the rank sort's scatter buffer (merge_window(k) <= CSA_MAX_K keys)
+  uint32_t rank_hist[kRankBins], rank_cur[kRankBins];
   int32_t offs[kMergeSlots];  // exclusive prefix of the row's slot counts
   SelectShared sel;
 };
+
+// Sorts the n <= merge_window(k) candidates descending: by rank over value bins,
+// or by the sorting network when the values crowd into a few bins.
+__device__ __forceinline__ void merge_sort_desc(MergeSmem& S, int n, int tid) {
+  if (!rank_sort_desc<kMergeThreads, kRankBins>(S.cand, n, S.scratch, S.rank_hist, S.rank_cur, &S.sel.part[0][0], 0,
+                                                tid))
+    sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
+}
 
 // One CTA per query row: the row's segment slots each hold at most
 // loose_keep(k) keys, unsorted. They are gathered into shared memory (a row
@@ -1372,7 +1384,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
   shrink_if_above_reg<kMergeThreads, kMergeCap / kMergeThreads>(S.cand, S.scratch, window, P.k, window, &S.sel, 0,
                                                                 tid);
   n = static_cast<int>(S.sel.n);
-  sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
+  merge_sort_desc(S, n, tid);
   for (int j = tid; j < P.k; j += kMergeThreads) {
     const int64_t o = static_cast<int64_t>(b) * P.k + j;
     if (j < n) {
@@ -1438,7 +1450,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lists_kernel(const MergeL
   shrink_if_above_reg<kMergeThreads, kMergeCap / kMergeThreads>(S.cand, S.scratch, window, A.k, window, &S.sel, 0,
                                                                 tid);
   const int n = static_cast<int>(S.sel.n);
-  sort_prefix_desc<kMergeThreads>(S.cand, n, 0, tid);
+  merge_sort_desc(S, n, tid);
   for (int j = tid; j < A.k; j += kMergeThreads) {
     const int64_t o = static_cast<int64_t>(b) * A.k + j;
     if (j < n) {

@@ -380,15 +380,17 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Four e2m1 codes (the nibbles of c16, element i in nibble i) as four e4m3 bytes
-// (element i in byte i) through the table (lo, hi): the magnitude by a byte-permute
-// lookup on the low three bits of each nibble, the sign from bit 3 (a permute of
-// 0x80 bytes in sign-replicate mode gives 0xFF for a set bit and 0x80 otherwise;
-// xor 0x80 and plus 1 per byte leave 0x80 or 0x01, no carry between bytes).
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t c16, uint32_t lo, uint32_t hi) {
-  const uint32_t mag = prmt(lo, hi, c16 & 0x7777u);
-  const uint32_t rep = prmt(0x80808080u, 0x80808080u, c16 & 0xFFFFu);
-  return mag | (((rep ^ 0x80808080u) + 0x01010101u) & 0x80808080u);
+// Four e2m1 codes (the low four nibbles of c, element i in nibble i; the
+// selector of a default-mode byte permute reads only bits 0-15) as four e4m3
+// bytes (element i in byte i) through the table (lo, hi): the magnitude by a
+// byte-permute lookup on the low three bits of each nibble, the sign from bit 3
+// (a permute of 0x80 bytes in sign-replicate mode gives 0xFF for a set bit and
+// 0x80 otherwise, so bit 6 of each byte is the sign: one shift moves it to bit 7;
+// the carry-out of each byte lands in bit 0 of the next, which the mask drops).
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t c, uint32_t lo, uint32_t hi) {
+  const uint32_t mag = prmt(lo, hi, c & 0x7777u);
+  const uint32_t rep = prmt(0x80808080u, 0x80808080u, c);
+  return mag | ((rep << 1) & 0x80808080u);
 }
 
 // Words r .. r + 15 of the 20 loaded (the record's code bytes) into c; word
@@ -442,7 +444,7 @@ __device__ __forceinline__ uint32_t stage_record_fp4(const uint8_t* row, int r, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t cw = c[4 * b + j];
-      v[8 * b + 2 * j] = e2m1x4_to_e4m3(cw & 0xFFFFu, lo, hi);
+      v[8 * b + 2 * j] = e2m1x4_to_e4m3(cw, lo, hi);
       v[8 * b + 2 * j + 1] = e2m1x4_to_e4m3(cw >> 16, lo, hi);
     }
   }

@@ -584,6 +584,104 @@ __device__ void sort_regs_desc(uint64_t* keys, int m, int bar, int gtid) {
   named_bar_sync(bar, NT);
 }
 
+// Sorts keys[0, n) into descending order by rank: the keys are counted into NB
+// bins of equal width over their value words (bin 0 the highest), scattered by
+// bin into tmp (n entries), and each key's place is its bin's offset plus the
+// number of keys of its bin that order before it (greater, or equal and
+// scattered earlier). A few barriers instead of a sorting network's dependent
+// stages; a bin's keys compare only among themselves. Returns false, having
+// moved nothing, when some bin holds more than kRankCrowd keys (many equal or
+// nearly equal values), where a sorting network is cheaper. hist and cur are
+// NB-entry arrays (after the scatter, cur is each bin's end), red holds
+// 2 * NT / 32 words.
+constexpr int kRankCrowd = 48;
+template <int NT, int NB>
+__device__ bool rank_sort_desc(uint64_t* keys, int n, uint64_t* tmp, uint32_t* hist, uint32_t* cur, uint32_t* red,
+                               int bar, int gtid) {
+  static_assert(NB % NT == 0 && NT % 32 == 0, "whole bins per thread");
+  constexpr int NW = NT / 32, BPT = NB / NT;
+  const int lane = gtid & 31, warp = gtid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0;
+  for (int i = gtid; i < n; i += NT) {
+    const uint32_t v = static_cast<uint32_t>(keys[i] >> 32);
+    lo = min(lo, v);
+    hi = max(hi, v);
+  }
+  lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (lane == 0) {
+    red[warp] = lo;
+    red[NW + warp] = hi;
+  }
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) hist[BPT * gtid + j] = 0;
+  named_bar_sync(bar, NT);
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, red[w]);
+    hi = max(hi, red[NW + w]);
+  }
+  constexpr int kBits = NB == 256 ? 8 : NB == 512 ? 9 : NB == 1024 ? 10 : 11;
+  static_assert(NB == (1 << kBits), "NB is 256, 512, 1024 or 2048");
+  const int s = hi > lo ? max(0, 32 - kBits - __clz(hi - lo)) : 0;  // (hi - lo) >> s < NB
+  auto bin_of = [&](uint64_t key) {
+    return static_cast<uint32_t>(NB - 1) - ((static_cast<uint32_t>(key >> 32) - lo) >> s);
+  };
+  for (int i = gtid; i < n; i += NT) atomicAdd(&hist[bin_of(keys[i])], 1u);
+  named_bar_sync(bar, NT);
+  // exclusive scan over the bins (highest values first) and the fullest bin
+  uint32_t c[BPT], sum = 0, most = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    c[j] = hist[BPT * gtid + j];
+    sum += c[j];
+    most = max(most, c[j]);
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  most = __reduce_max_sync(0xFFFFFFFFu, most);
+  if (lane == 31) red[warp] = incl;  // lo and hi were read before the last barrier
+  if (lane == 0) red[NW + warp] = most;
+  named_bar_sync(bar, NT);
+  uint32_t before = 0;
+  most = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    before += w < warp ? red[w] : 0u;
+    most = max(most, red[NW + w]);
+  }
+  if (most > static_cast<uint32_t>(kRankCrowd)) return false;  // uniform
+  uint32_t run = before + incl - sum;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    cur[BPT * gtid + j] = run;
+    run += c[j];
+  }
+  named_bar_sync(bar, NT);
+  for (int i = gtid; i < n; i += NT) {
+    const uint64_t key = keys[i];
+    tmp[atomicAdd(&cur[bin_of(key)], 1u)] = key;
+  }
+  named_bar_sync(bar, NT);
+  for (int p = gtid; p < n; p += NT) {
+    const uint64_t key = tmp[p];
+    const uint32_t d = bin_of(key), b1 = cur[d], b0 = b1 - hist[d];
+    uint32_t r = 0;
+#pragma unroll 4
+    for (uint32_t j = b0; j < b1; ++j) {
+      const uint64_t o = tmp[j];
+      r += (o > key || (o == key && j < static_cast<uint32_t>(p))) ? 1u : 0u;
+    }
+    keys[b0 + r] = key;
+  }
+  named_bar_sync(bar, NT);
+  return true;
+}
+
 // Sorts keys[0, n) in descending order in place; keys[n, m) are overwritten with
 // zero padding, where m is the power of two >= max(n, 64) (the buffer must hold
 // m keys). Up to 8 * NT keys are sorted in registers (sort_regs_desc).
