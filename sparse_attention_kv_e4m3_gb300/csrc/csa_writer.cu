@@ -6,11 +6,27 @@
 // nearest e4m3 value with ties to even and saturating at 448; a row whose
 // scale is 0 (all zero, or amax / 448 underflows) is zero codes and scale 0.
 //
-// A warp quantises a row at a time (32 rows per pass, their loads in flight
-// together): each lane holds 4 of the 128 values, a shuffle tree finds amax,
-// and each lane stores its 4 codes as one 32-bit word (records are 4-byte
-// aligned); lane 0 stores the scale. Memory-bound: the row is read once,
-// coalesced, and the record written once.
+// Eight lanes quantise a row (a warp four rows at a time): each lane holds 16 of
+// the 128 values, a reduction over the group's magnitude bits gives amax and
+// tells whether all are finite, and each lane stores its 16 codes as four
+// 32-bit words (records are 4-byte aligned); the group's first lane stores the
+// scale. The per-row work (amax, the scale, its reciprocal) is thus shared by
+// eight lanes instead of a whole warp. The row is read once, coalesced, and the
+// record written once.
+//
+// The quotients x / scale are the correctly rounded binary32 ones, computed
+// without a division per value: with y = RN(1/scale) (one correctly rounded
+// reciprocal per row), q0 = RN(x y) is within a few ulps of x / scale; one
+// correction q1 = RN(q0 + RN(x - q0 scale) y) brings it within one ulp, and a
+// second one (the same step from q1) gives RN(x / scale) by Markstein's theorem
+// on FMA-based division (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; restated
+// in Muller et al., "Handbook of Floating-Point Arithmetic", the section on
+// Newton-Raphson-based division with an FMA): the residuals x - q scale are
+// exact under an FMA when nothing underflows. That holds for every quotient
+// that can reach a nonzero code (|x / scale| >= 2^-10, so |x| >= 2^-100) once
+// scale >= 2^-90; smaller scales take the division itself. Quotients below
+// 2^-10 become a signed zero code either way.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -38,86 +54,155 @@ struct WriteParams {
   int32_t* dev_status;
 };
 
-// Row i's record address, or the CSA_DEV_* bit that stops it (checked in the
+// Row i's request and position words (an index past the rows reads row 0's,
+// which the caller drops), loaded without a branch on any loaded value so that
+// they stay in flight while the warp works on earlier rows.
+struct RowRef {
+  int32_t req, pos;
+};
+
+__device__ __forceinline__ RowRef row_ref(const WriteParams& W, int64_t i) {
+  const int64_t k = i < W.n ? i : 0;
+  return {W.row_req ? W.row_req[k] : static_cast<int32_t>(k), W.row_pos[k]};
+}
+
+__device__ __forceinline__ bool ref_in_range(const WriteParams& W, RowRef r) {
+  return r.req >= 0 && r.req < W.num_req && r.pos >= 0 && r.pos < static_cast<int64_t>(kPage) * W.pt_stride;
+}
+
+// The row's page-table word (the table's first word when the request or the
+// position is out of range: record_at then flags the row).
+__device__ __forceinline__ int32_t page_word(const WriteParams& W, RowRef r) {
+  return W.page_table[ref_in_range(W, r) ? static_cast<int64_t>(r.req) * W.pt_stride + r.pos / kPage : 0];
+}
+
+// The row's record address, or the CSA_DEV_* bit that stops it (checked in the
 // documented order: request, position, page).
-__device__ __forceinline__ int32_t record_of(const WriteParams& W, int64_t i, uint8_t** rec) {
-  const int64_t req = W.row_req ? W.row_req[i] : i;
-  if (req < 0 || req >= W.num_req) return CSA_DEV_BAD_REQUEST;
-  const int32_t pos = W.row_pos[i];
-  if (pos < 0 || pos >= static_cast<int64_t>(kPage) * W.pt_stride) return CSA_DEV_LEN_OOB;
-  const int64_t phys = W.page_table[req * W.pt_stride + pos / kPage];
+__device__ __forceinline__ int32_t record_at(const WriteParams& W, RowRef r, int32_t phys, uint8_t** rec) {
+  if (r.req < 0 || r.req >= W.num_req) return CSA_DEV_BAD_REQUEST;
+  if (r.pos < 0 || r.pos >= static_cast<int64_t>(kPage) * W.pt_stride) return CSA_DEV_LEN_OOB;
   if (phys < 0 || phys >= W.num_pages) return CSA_DEV_PAGE_OOB;
-  *rec = W.kv + phys * W.page_stride + static_cast<int64_t>(pos % kPage) * kRec;
+  *rec = W.kv + static_cast<int64_t>(phys) * W.page_stride + static_cast<int64_t>(r.pos % kPage) * kRec;
   return 0;
 }
 
-// A warp takes 32 rows per pass: each lane resolves one row's record (request,
-// position, page table) so that those loads are in flight together; then the
-// rows' values are loaded kChunk rows at a time, every lane holding 4 values of
-// each, and each row is quantised and stored.
-constexpr int kRowsPerPass = 32, kChunk = 8;
+// A warp takes 32 rows per pass, each lane resolving one row's record; the
+// resolution runs ahead of the quantisation: while a pass is quantised, the
+// page-table words of the next pass and the request and position words of the
+// one after are in flight. The pass is quantised four rows (one per eight-lane
+// group) per step, the loads of several steps in flight together.
+constexpr int kRowsPerPass = 32;  // one row's record resolved per lane
+constexpr int kRowLanes = 8, kVals = kD / kRowLanes;  // lanes per row, values per lane
 constexpr int32_t kNoRow = 1 << 30;
 
-__device__ __forceinline__ void load_row(const WriteParams& W, int64_t i, int lane, float (&x)[4]) {
-  if (W.bf16) {
-    const uint2 raw = reinterpret_cast<const uint2*>(W.keys)[i * (kD / 4) + lane];
-    x[0] = __uint_as_float(raw.x << 16);
-    x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-    x[2] = __uint_as_float(raw.y << 16);
-    x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-  } else {
-    const float4 v = reinterpret_cast<const float4*>(W.keys)[i * (kD / 4) + lane];
-    x[0] = v.x;
-    x[1] = v.y;
-    x[2] = v.z;
-    x[3] = v.w;
+// The 16 values of row i that lane s of the row's group holds (d = 16 s .. 16 s + 15).
+template <bool kBf16>
+struct RowSlice {
+  static constexpr int kWords = kBf16 ? 2 : 4;  // 16-byte loads per lane
+  uint4 raw[kWords];
+  __device__ __forceinline__ void load(const WriteParams& W, int64_t i, int sl) {
+    const uint4* base = reinterpret_cast<const uint4*>(W.keys) + i * (kWords * kRowLanes) + kWords * sl;
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) raw[k] = base[k];
   }
+  __device__ __forceinline__ void values(float (&v)[kVals]) const {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
+#pragma unroll
+    for (int k = 0; k < kVals; ++k) {
+      if constexpr (kBf16)
+        v[k] = __uint_as_float((k & 1) ? (w[k >> 1] & 0xFFFF0000u) : (w[k >> 1] << 16));
+      else
+        v[k] = __uint_as_float(w[k]);
+    }
+  }
+};
+
+// RN(x / b) from y = RN(1 / b) by two FMA corrections (see the file header);
+// b >= 2^-90, finite. The quotient takes x's sign (b > 0): a zero x gives a zero
+// residual, whose sum with -0 would otherwise round to +0.
+__device__ __forceinline__ float quotient_rn(float x, float b, float y) {
+  const float q0 = x * y;
+  const float q1 = fmaf(fmaf(-q0, b, x), y, q0);
+  return copysignf(fmaf(fmaf(-q1, b, x), y, q1), x);
 }
 
+template <bool kBf16>
 __global__ void __launch_bounds__(kWriterThreads) write_keys_kernel(const WriteParams W) {
-  const int lane = threadIdx.x & 31;
+  constexpr int kStepRows = 32 / kRowLanes;          // rows a warp quantises at once
+  constexpr int kChunkSteps = kBf16 ? 4 : 2;         // steps whose loads are in flight together
+  constexpr int kSteps = kRowsPerPass / kStepRows;   // steps per pass
+  const int lane = threadIdx.x & 31, g = lane / kRowLanes, sl = lane % kRowLanes;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (kWriterThreads / 32);
   int32_t flags = 0;
-  for (int64_t i0 = ((static_cast<int64_t>(blockIdx.x) * kWriterThreads + threadIdx.x) >> 5) * kRowsPerPass;
-       i0 < W.n; i0 += warps * kRowsPerPass) {
+  const int64_t step = warps * kRowsPerPass;
+  int64_t i0 = ((static_cast<int64_t>(blockIdx.x) * kWriterThreads + threadIdx.x) >> 5) * kRowsPerPass;
+  RowRef r0 = row_ref(W, i0 + lane), r1 = row_ref(W, i0 + step + lane);
+  int32_t pg0 = page_word(W, r0);
+  for (; i0 < W.n; i0 += step) {
+    const RowRef r2 = row_ref(W, i0 + 2 * step + lane);
+    const int32_t pg1 = page_word(W, r1);
     uint8_t* my_rec = nullptr;
-    const int32_t my_f = i0 + lane < W.n ? record_of(W, i0 + lane, &my_rec) : kNoRow;
+    const int32_t my_f = i0 + lane < W.n ? record_at(W, r0, pg0, &my_rec) : kNoRow;
+    r0 = r1;
+    r1 = r2;
+    pg0 = pg1;
     const int rows = W.n - i0 < kRowsPerPass ? static_cast<int>(W.n - i0) : kRowsPerPass;  // uniform
-    for (int c = 0; c < rows; c += kChunk) {
-      float x[kChunk][4];
+    for (int c = 0; c < kSteps; c += kChunkSteps) {
+      RowSlice<kBf16> x[kChunkSteps];
 #pragma unroll
-      for (int r = 0; r < kChunk; ++r) load_row(W, c + r < rows ? i0 + c + r : i0, lane, x[r]);
+      for (int j = 0; j < kChunkSteps; ++j) {
+        const int r = kStepRows * (c + j) + g;  // this group's row of the step, within the pass
+        x[j].load(W, r < rows ? i0 + r : i0, sl);
+      }
 #pragma unroll
-      for (int r = 0; r < kChunk; ++r) {
-        if (c + r >= rows) break;  // uniform
-        const int32_t f0 = __shfl_sync(0xFFFFFFFFu, my_f, c + r);
-        uint8_t* rec =
-            reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(my_rec), c + r));
+      for (int j = 0; j < kChunkSteps; ++j) {
+        const int r = kStepRows * (c + j) + g;
+        const int32_t f0 = __shfl_sync(0xFFFFFFFFu, my_f, r);
+        uint8_t* rec = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(my_rec), r));
+        float v[kVals];
+        x[j].values(v);
+        // magnitude bits order like the magnitudes; at or above 0x7F800000: inf or NaN
+        uint32_t mbits = 0;
+#pragma unroll
+        for (int k = 0; k < kVals; ++k) mbits = max(mbits, __float_as_uint(v[k]) & 0x7FFFFFFFu);
+#pragma unroll
+        for (int o = 1; o < kRowLanes; o <<= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
+        if (r >= rows) continue;  // the group's row is past the last one
         int32_t f = f0;
-        const bool finite = isfinite(x[r][0]) && isfinite(x[r][1]) && isfinite(x[r][2]) && isfinite(x[r][3]);
-        if (f == 0 && !__all_sync(0xFFFFFFFFu, finite)) f = CSA_DEV_RANGE;
-        if (f != 0) {  // uniform
+        if (f == 0 && mbits >= 0x7F800000u) f = CSA_DEV_RANGE;
+        if (f != 0) {  // uniform over the group
           flags |= f;
           continue;
         }
-        float amax = fmaxf(fmaxf(fabsf(x[r][0]), fabsf(x[r][1])), fmaxf(fabsf(x[r][2]), fabsf(x[r][3])));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float amax = __uint_as_float(mbits);
         const float scale = amax / 448.0f;  // IEEE division, round to nearest even
-        uint32_t word = 0;
+        uint32_t word[kVals / 4] = {};
         if (scale > 0.0f) {  // a scale of 0 (amax == 0, or amax / 448 underflows): zero codes
-          const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-              make_float2(x[r][0] / scale, x[r][1] / scale), __NV_SATFINITE, __NV_E4M3);
-          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-              make_float2(x[r][2] / scale, x[r][3] / scale), __NV_SATFINITE, __NV_E4M3);
-          word = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+          if (scale >= 0x1p-90f) {  // uniform over the group
+            const float y = __frcp_rn(scale);
+#pragma unroll
+            for (int k = 0; k < kVals; ++k) v[k] = quotient_rn(v[k], scale, y);
+          } else {
+#pragma unroll
+            for (int k = 0; k < kVals; ++k) v[k] = v[k] / scale;
+          }
+#pragma unroll
+          for (int k = 0; k < kVals / 4; ++k) {
+            const __nv_fp8x2_storage_t lo =
+                __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k], v[4 * k + 1]), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi =
+                __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k + 2], v[4 * k + 3]), __NV_SATFINITE, __NV_E4M3);
+            word[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+          }
         }
         uint32_t* rw = reinterpret_cast<uint32_t*>(rec);
-        rw[lane] = word;  // bytes 4 lane .. 4 lane + 3: codes of d = 4 lane .. 4 lane + 3
-        if (lane == 0) rw[kD / 4] = __float_as_uint(scale);  // little-endian fp32 at byte 128
+#pragma unroll
+        for (int k = 0; k < kVals / 4; ++k) rw[(kVals / 4) * sl + k] = word[k];  // codes of d = 16 sl ..
+        if (sl == 0) rw[kD / 4] = __float_as_uint(scale);  // little-endian fp32 at byte 128
       }
     }
   }
+  flags = static_cast<int32_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(flags)));
   if (flags && W.dev_status && lane == 0) atomicOr(W.dev_status, flags);
 }
 
@@ -155,13 +240,13 @@ extern "C" csa_status csa_index_write_keys(const csa_write_args* a, void* stream
   W.pt_stride = a->pt_stride;
   W.dev_status = a->dev_status;
   int per_sm = 0;  // resident CTAs per SM: one full wave, grid-stride beyond
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, write_keys_kernel, kWriterThreads, 0) != cudaSuccess ||
-      per_sm < 1)
+  const auto kernel = W.bf16 ? write_keys_kernel<true> : write_keys_kernel<false>;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWriterThreads, 0) != cudaSuccess || per_sm < 1)
     return CSA_ERR_CUDA;
   const int64_t rows_per_block = kRowsPerPass * (kWriterThreads / 32);
   const int64_t want = (a->n + rows_per_block - 1) / rows_per_block;
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  write_keys_kernel<<<grid, kWriterThreads, 0, static_cast<cudaStream_t>(stream)>>>(W);
+  kernel<<<grid, kWriterThreads, 0, static_cast<cudaStream_t>(stream)>>>(W);
   return cudaGetLastError() == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }

@@ -122,6 +122,59 @@ def test_special_rows():
     assert np.array_equal(got, want), np.argwhere(got != want)[:5]
 
 
+def _scales_with_all_ones_significand(rng, count):
+    """amax values whose scale RN(amax / 448) has the all-ones significand
+    (2 - 2^-23) 2^e, the hardest divisor for a reciprocal-based quotient."""
+    out = []
+    while len(out) < count:
+        e = int(rng.integers(-88, 100))
+        target = np.float32(np.ldexp(2.0 - 2.0 ** -23, e))
+        a = np.float32(np.float64(target) * 448.0)
+        for _ in range(8):
+            if np.float32(a / np.float32(448.0)) == target:
+                out.append(a)
+                break
+            a = np.nextafter(a, np.float32(np.inf) if a / np.float32(448.0) < target else np.float32(0))
+    return np.array(out, dtype=np.float32)
+
+
+def test_quotients_at_code_boundaries():
+    """x / scale within a few binary32 ulps of every e4m3 rounding boundary
+    (midpoints between codes, the 448/464 saturation edge, the 2^-10 edge of
+    the smallest code), at scales from 2^-96 to 2^110 (both sides of the
+    writer's 2^-90 switch from reciprocal-based quotients to the division) and
+    at divisors with an all-ones significand: the codes must be the oracle's,
+    whose quotients are IEEE binary32 divisions."""
+    rng = np.random.default_rng(11)
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    grid = grid.astype(np.float64)
+    bounds = np.concatenate([(grid[:-1] + grid[1:]) / 2, grid[1:], [2.0 ** -10, 2.0 ** -9, 440.0]])
+    bounds = bounds[bounds <= 440.0]
+    n = 8192
+    amax = np.ldexp(rng.uniform(1.0, 2.0, n), rng.integers(-87, 118, n)).astype(np.float32)
+    amax[: n // 8] = _scales_with_all_ones_significand(rng, n // 8)
+    # scales around 2^-90, the switch: amax = 448 scale
+    amax[n // 8: n // 8 + 256] = np.ldexp(rng.uniform(1.0, 2.0, 256), rng.integers(-84, -78, 256)).astype(np.float32)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    m = rng.choice(bounds, size=(n, D))
+    sign = np.where(rng.random((n, D)) < 0.5, -1.0, 1.0)
+    ulps = rng.integers(-3, 4, size=(n, D))
+    x = (sign * m * scale[:, None].astype(np.float64)).astype(np.float32)
+    up, down = np.float32(np.inf), np.float32(-np.inf)
+    for _ in range(3):  # up to three ulps away in either direction
+        x = np.where(ulps > 0, np.nextafter(x, up), np.where(ulps < 0, np.nextafter(x, down), x))
+        ulps = ulps - np.sign(ulps)
+    x[:, 0] = amax  # the largest magnitude of each row, so its scale is the one above
+    kv, pt = _cache(num_req=8, pages_per_req=16, seed=12)
+    req, pos = _distinct_positions(8, 16, n, seed=13)
+    want = kv.copy()
+    assert oracle.write_keys(x, req, pos, want, pt) == 0
+    got, status = _write_gpu(x, req, pos, kv, pt)
+    assert status == 0
+    bad = np.argwhere(got != want)
+    assert len(bad) == 0, bad[:5]
+
+
 def test_invalid_rows_are_flagged_and_skipped():
     kv, pt = _cache(num_req=2, pages_per_req=2, seed=5)
     pt[1, 1] = kv.shape[0] + 4  # a page id out of range
