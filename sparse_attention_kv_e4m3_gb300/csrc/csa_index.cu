@@ -857,6 +857,21 @@ __device__ void role_qprep(const Params& P, Smem<H>& S) {
   prep_segments<H, kTilePages>(P, S);
 }
 
+// Packed fp32 pairs (two IEEE binary32 operations per instruction, round to nearest).
+__device__ __forceinline__ uint64_t f2pack_(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack_(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma_(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 // One warp of a worker group: TMEM lane quarter q of every tile the group owns
 // (tiles i with i % kWorkerGroups == group). It moves its records' key bytes
 // (32 rows of each of the kSub sub-tiles) from the staged pages into the TMEM
@@ -959,42 +974,35 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
   };
 
   // Logit of this lane's record in the sub-tile whose accumulator is stage td
-  // (sub-staged accumulators): two 16-head chunks per TMEM wait, two sums.
+  // (sub-staged accumulators): two 16-head chunks per TMEM wait, four packed
+  // pairs of sums (two fp32 multiply-adds per instruction).
   auto logit_one = [&](int td, uint32_t scb, int seg) -> float {
     const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
     const float s = __uint_as_float(scb);
     const float g = s < 0.0f ? -1.0f : 1.0f;
     const bool all_pos = __all_sync(0xFFFFFFFFu, g > 0.0f);
-    float a0[8], a1[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) a0[j] = a1[j] = 0.f;
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll 1
     for (int c = 0; c < H; c += 32) {  // heads c .. c+31
-      uint32_t x0[16], x1[16];
-      tmem_ld16(tmem + d_col<H>(td) + c + lane_off, x0);
-      tmem_ld16(tmem + d_col<H>(td) + c + 16 + lane_off, x1);
+      uint32_t x[32];
+      tmem_ld16(tmem + d_col<H>(td) + c + lane_off, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+      tmem_ld16(tmem + d_col<H>(td) + c + 16 + lane_off, *reinterpret_cast<uint32_t(*)[16]>(&x[16]));
       tmem_wait_ld();
-      float4 w4[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w4[j] = wv[(c >> 2) + j];
-      const float* w = reinterpret_cast<const float*>(w4);
-      if (all_pos) {
+      for (int j = 0; j < 8; ++j) {
+        const float4 wq = wv[(c >> 2) + j];
+        float a[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          a0[j & 7] = fmaf(fmaxf(__uint_as_float(x0[j]), 0.f), w[j], a0[j & 7]);
-          a1[j & 7] = fmaf(fmaxf(__uint_as_float(x1[j]), 0.f), w[16 + j], a1[j & 7]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          a0[j & 7] = fmaf(fmaxf(g * __uint_as_float(x0[j]), 0.f), w[j], a0[j & 7]);
-          a1[j & 7] = fmaf(fmaxf(g * __uint_as_float(x1[j]), 0.f), w[16 + j], a1[j & 7]);
-        }
+        for (int i = 0; i < 4; ++i) a[i] = all_pos ? __uint_as_float(x[4 * j + i]) : g * __uint_as_float(x[4 * j + i]);
+        acc[(2 * j) & 3] = f2fma_(f2pack_(fmaxf(a[0], 0.f), fmaxf(a[1], 0.f)), f2pack_(wq.x, wq.y), acc[(2 * j) & 3]);
+        acc[(2 * j + 1) & 3] =
+            f2fma_(f2pack_(fmaxf(a[2], 0.f), fmaxf(a[3], 0.f)), f2pack_(wq.z, wq.w), acc[(2 * j + 1) & 3]);
       }
     }
+    float p[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a0[j] += a1[j];
-    return fabsf(s) * (((a0[0] + a0[4]) + (a0[1] + a0[5])) + ((a0[2] + a0[6]) + (a0[3] + a0[7])));
+    for (int i = 0; i < 4; ++i) f2unpack_(acc[i], p[2 * i], p[2 * i + 1]);
+    return fabsf(s) * (((p[0] + p[4]) + (p[1] + p[5])) + ((p[2] + p[6]) + (p[3] + p[7])));
   };
 
   // Sub-staged accumulators: the first sub-tile's logit, read and its stage freed
