@@ -38,14 +38,20 @@ sys.path.insert(0, ROOT)
 METRIC = "CSA indexer keys scored/s and HBM GB/s (fraction of peak), score+top-512"
 UNIT = "keys/s"
 K_TOP = 512
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_long_ragged_decode.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "sparse_attention_kv_e4m3_gb300", "csrc", f)
+CSRC = os.path.join(ROOT, "sparse_attention_kv_e4m3_gb300", "csrc")
+KERNEL_SOURCES = [os.path.join(CSRC, f)
                   for f in ("csa_index.cu", "csa_score64.cuh", "csa_ptx.cuh", "csa_select.cuh", "csa_internal.h")]
+# committed ncu summary per bench leg: (file under profiles/, the sources its kernel is built from)
+PROFILES = {
+    "index": ("score_kernel_long_ragged_decode.md", KERNEL_SOURCES),
+    "fp4": ("score_kernel_long_ragged_decode_mxfp4.md", KERNEL_SOURCES),
+    "write_keys": ("write_keys_long_ragged_cache.md", [os.path.join(CSRC, "csa_writer.cu")]),
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(paths=None) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in paths or KERNEL_SOURCES:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -61,11 +67,14 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the scoring kernel from the committed ncu summary,
-    or None if the kernel sources changed since that capture."""
+def profiled_traffic(leg: str = "index"):
+    """DRAM bytes per launch of the leg's kernel from its committed ncu summary,
+    or None if there is none or the kernel's sources changed since that capture."""
+    if leg not in PROFILES:
+        return None
+    name, sources = PROFILES[leg]
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     vals = {}
@@ -74,7 +83,7 @@ def profiled_traffic():
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(sources):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -471,7 +480,7 @@ def run_native(args):
 
     peak, peak_src = measured_peaks()
     achieved = alg_bytes / (phase1_ms / 1e3) / 1e9
-    traffic = profiled_traffic() if args.op == "index" else None
+    traffic = profiled_traffic(args.op)
     line = {
         "metric": METRIC if args.op == "index" else METRIC + ", MXFP4 records", "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps,
@@ -608,7 +617,8 @@ def run_write_keys(args, emit: bool = True):
         "config": {"workload": f"{args.workload} cache rewritten", "rows": n,
                    "l2": "inputs and cache larger than L2; no flush"},
         "roofline": {"kernel": "write_keys_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
-                     "peak_source": f"{src} hbm_gbs", "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                     "peak_source": f"{src} hbm_gbs", "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": profiled_traffic("write_keys"),
                      "algorithmic_bytes_per_launch": alg},
         "clocks": clocks,
         "gpu_launches": steps,
