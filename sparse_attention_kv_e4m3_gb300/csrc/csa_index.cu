@@ -1020,7 +1020,7 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
   // Epilogue of own tile i of row b, local tile lt, segment `seg`; the caller
   // has seen the tile's accumulator complete.
   auto epilogue = [&](int64_t i, int32_t b, int64_t lt, int seg, const uint32_t (&sc)[kSub],
-                      const uint32_t (&pos)[kSub], float logit0) -> bool {
+                      const uint32_t (&pos)[kSub], float logit0, const float (&prev)[kSub]) -> bool {
     tc_fence_after();
     float logit[kSub];
     if constexpr (Geo<H>::kSubStaged) {
@@ -1047,7 +1047,7 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
         if (!isnan(__uint_as_float(sc[sub]))) {
           const float v = P.raw_logits ? logit[sub] : __frcp_rn(1.0f + __expf(-logit[sub]));
           float* o = out + kMmaRows * sub;
-          *o = P.fold == 0 ? v : (P.fold == CSA_FOLD_MAX ? fmaxf(*o, v) : *o + v);
+          *o = P.fold == 0 ? v : (P.fold == CSA_FOLD_MAX ? fmaxf(prev[sub], v) : prev[sub] + v);
         }
     } else {
       const int slot = static_cast<int>(i % kKeyRing);
@@ -1100,13 +1100,24 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
       const bool okd = mbar_wait(smem_u32(&S.dfull[t % kDSignals]), static_cast<uint32_t>((t / kDSignals) & 1),
                                  &S.abort_flag);
       if (!__all_sync(0xFFFFFFFFu, okd)) break;
+      // a fold reads the plane's current values: issue those loads now, so that they
+      // arrive while the accumulators are read and the next tile is staged
+      float prev[kSub] = {0.0f, 0.0f};
+      if constexpr (!kTopk) {
+        if (P.fold != 0) {
+          const float* out = P.scores + static_cast<int64_t>(cur.b) * P.score_stride + cur.lt * kTile + row;
+#pragma unroll
+          for (int sub = 0; sub < kSub; ++sub)
+            if (!isnan(__uint_as_float(cur_sc[sub]))) prev[sub] = out[kMmaRows * sub];
+        }
+      }
       float logit0 = 0.0f;
       if constexpr (Geo<H>::kSubStaged) logit0 = first_half(t, cur_sc[0], seg);
       if (t + kWorkerGroups < nt) {
         ok = load(t + kWorkerGroups, nxt_sc, nxt_pos);
         if (!ok) break;
       }
-      ok = epilogue(t, cur.b, cur.lt, seg, cur_sc, cur_pos, logit0);
+      ok = epilogue(t, cur.b, cur.lt, seg, cur_sc, cur_pos, logit0, prev);
 #pragma unroll
       for (int u = 0; u < kSub; ++u) {
         cur_sc[u] = nxt_sc[u];
