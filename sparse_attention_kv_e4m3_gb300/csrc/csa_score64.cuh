@@ -821,10 +821,10 @@ __device__ void role_select(const Params& P, Smem& S) {
     }
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
-    shrink_if_above_reg<128, kCapW / 128>(S.cand, S.scratch, kCapW - kTileRecs, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+    shrink_if_above_reg<128, kCapW / 128, 512>(S.cand, S.scratch, kCapW - kTileRecs, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
     const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
     if (seg_end) {
-      shrink_if_above_reg<128, kCapW / 128>(S.cand, S.scratch, loose_keep(P.k), P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+      shrink_if_above_reg<128, kCapW / 128, 512>(S.cand, S.scratch, loose_keep(P.k), P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
       const int n = static_cast<int>(S.sel.n);
       uint8_t* out = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
       uint64_t* ent = reinterpret_cast<uint64_t*>(out + 16);
