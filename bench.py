@@ -104,6 +104,7 @@ def algorithmic_bytes(w) -> int:
 
 
 HEADS, HEAD_DIM = 64, 128
+NOMINAL_HBM_GBS = 7900.0  # GB300's nominal HBM3e bandwidth, reported beside the measured copy peak
 PER_CONFIG = ("tiny_decode", "decode_batch", "resident_1m", "prefill_chunk")
 
 
@@ -171,6 +172,7 @@ def measure_configs(names, dev, steps: int = 20):
         keys, nbytes, flops = int(w.visible_counts().sum()), algorithmic_bytes(w), algorithmic_flops(w)
         rec = {"us": ms * 1e3, "queries": w.num_q, "records": keys, "keys_per_s": keys / (ms / 1e3),
                "gbs": nbytes / (ms / 1e3) / 1e9, "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
+               "frac_of_nominal": nbytes / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                "algorithmic_bytes": nbytes, "flops": flops, "tflops": flops / (ms / 1e3) / 1e12}
         if name.startswith("prefill"):
             rec["tensor_frac"] = rec["tflops"] / (2.0 * bf16)
@@ -498,7 +500,10 @@ def run_native(args):
                                 "w64::score_kernel_w64<topk, mxfp4> (scoring phase)"), "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "phase1_ms": phase1_ms,
-                     "algorithmic_bytes_per_launch": alg_bytes},
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "step_frac": alg_bytes / (ms_max / 1e3) / 1e9 / peak,
+                     "step_note": "step_frac: the whole step (scoring kernel and merge kernel) against the same peak"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "inputs": "q, fused_w, q_len, page_table copied from pinned host memory every step; "

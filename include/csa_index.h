@@ -175,7 +175,11 @@ const char* csa_status_str(csa_status s);
 
 /*
  * Bytes of device workspace that csa_index_topk and csa_index_score_topk_fused need for
- * these arguments and this k. Pure host arithmetic on num_q and k (no device access).
+ * these arguments and this k. Pure host arithmetic on num_q and k (no device access):
+ * 256-byte-rounded 4*(num_q+2) bytes of row offsets, then (num_q + CSA_MAX_CTAS)
+ * candidate slots of 16 + 8*min(1024, k + k/2) bytes rounded up to 16, or of
+ * 16 + 8*2048 bytes when num_q >= 512 (batches of that many rows take the scorer for
+ * short rows, which leaves a whole row of up to 2048 candidates uncut for the merge).
  * Returns 0 when num_q < 0 or k is outside [1, CSA_MAX_K].
  */
 size_t csa_index_workspace_bytes(const csa_index_args* args, int32_t k);

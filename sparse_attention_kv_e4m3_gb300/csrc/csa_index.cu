@@ -82,6 +82,8 @@ template <> struct Geo<128> {
   static constexpr bool kSubStaged = true;
 };
 constexpr int kRing = 4;       // page-walker ring slots of 32 pages
+constexpr int kSlotKeysMax = 2048;  // most keys a workspace slot has room for (see slot_bytes_fused)
+constexpr int32_t kShortRowsMin = 512;  // rows from which the fused path takes the short-row scorer
 constexpr int kCap = 2048;     // candidate buffer of one segment (keys)
 constexpr int kKeyRing = 8;    // tiles of ranking keys between the workers and the selector
 
@@ -1289,7 +1291,7 @@ namespace csa {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeCap = 4096;   // candidate buffer; a row with more is cut back between chunks of slots
 constexpr int kMergeSlots = CSA_MAX_CTAS + 1;
-static_assert(2 * CSA_MAX_K <= kMergeCap, "after a cut to merge_window(k), any slot must fit");
+static_assert(CSA_MAX_K + kSlotKeysMax <= kMergeCap, "after a cut to merge_window(k), any slot must fit");
 
 constexpr int kRankBins = 1024;  // bins of the final rank sort
 static_assert(kMergeThreads / 32 <= 8, "the rank sort's per-warp partials fit sel.part");
@@ -1322,7 +1324,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
   const int tid = threadIdx.x;
   const int32_t b = blockIdx.x;
   const int32_t* tile_off = reinterpret_cast<const int32_t*>(P.ws);
-  const int keep = loose_keep(P.k), window = merge_window(P.k);
+  const int cap = static_cast<int>((P.slot_bytes - 16) / 8), window = merge_window(P.k);
   if (tid == 0) {
     S.sel.n = 0;
     S.sel.tau = 0;
@@ -1352,7 +1354,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
         const int64_t c = c0 + j;
         if (cta_begin(c, total, P.grid) != cta_begin(c + 1, total, P.grid)) {
           cnt = *reinterpret_cast<const int32_t*>(slot_ptr(j));
-          cnt = cnt < 0 ? 0 : (cnt > keep ? keep : cnt);  // a slot never holds more than loose_keep(k)
+          cnt = cnt < 0 ? 0 : (cnt > cap ? cap : cnt);  // a slot never holds more than it has room for
         }
       }
       int incl = cnt;
@@ -1370,7 +1372,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params P, in
   // Gather whole slots while they fit, one warp per slot with four loads in
   // flight per lane; when the next slot would not fit, cut the buffer to at
   // most `window` keys (never below k) and go on. After a cut any slot fits:
-  // window + loose_keep(k) <= 2 * CSA_MAX_K <= kMergeCap.
+  // window + a slot's room <= CSA_MAX_K + kSlotKeysMax <= kMergeCap.
   const int warp = tid >> 5, lane = tid & 31;
   int n = 0;
   for (int j0 = 0; j0 < nslots;) {
@@ -1592,7 +1594,14 @@ std::mutex g_mu;
 int g_sms[kMaxDevices];
 bool g_ready[kMaxDevices];
 
+// A slot: a 16-byte header (the key count) and room for the keys. Segments are
+// cut to at most loose_keep(k) keys before they are written, except in the
+// short-row scorer (kShortRowsMin rows and more, on a caller's workspace),
+// whose slots take a whole uncut row of up to kSlotKeysMax keys.
 size_t slot_bytes_for(int32_t k) { return (16 + 8 * static_cast<size_t>(loose_keep(k)) + 15) & ~size_t(15); }
+size_t slot_bytes_fused(int32_t num_q, int32_t k) {
+  return num_q >= kShortRowsMin ? (16 + 8 * static_cast<size_t>(kSlotKeysMax) + 15) & ~size_t(15) : slot_bytes_for(k);
+}
 // tile_off[num_q + 2] (virtual prefix sums and the charge per row), then the slots
 size_t slots_offset_for(int32_t num_q) { return (4 * (static_cast<size_t>(num_q) + 2) + 255) & ~size_t(255); }
 
@@ -1647,6 +1656,9 @@ csa_status device_setup(int* sms) {
     if (cudaFuncSetAttribute(w64::score_kernel_w64<false, CSA_RECORD_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(w64::score_kernel_w64<true, CSA_RECORD_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(w64::score_kernel_w64<true, CSA_RECORD_E4M3, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(w64::kSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(w64::score_kernel_w64<false, CSA_RECORD_MXFP4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1707,6 +1719,8 @@ csa_status launch_w64(const Params& P, bool topk, int sms, cudaStream_t s) {
   const bool fp4 = P.fmt == CSA_RECORD_MXFP4;
   if (topk && fp4)
     w64::score_kernel_w64<true, CSA_RECORD_MXFP4><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
+  else if (topk && P.num_q >= kShortRowsMin)  // many rows: the short-row scorer
+    w64::score_kernel_w64<true, CSA_RECORD_E4M3, true><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
   else if (topk)
     w64::score_kernel_w64<true, CSA_RECORD_E4M3><<<sms, w64::kThreads, w64::kSmemBytes, s>>>(P);
   else if (fp4)
@@ -1745,7 +1759,7 @@ const char* csa_status_str(csa_status s) {
 size_t csa_index_workspace_bytes(const csa_index_args* args, int32_t k) {
   if (!args || args->num_q < 0 || k < 1 || k > CSA_MAX_K) return 0;
   return slots_offset_for(args->num_q) +
-         (static_cast<size_t>(args->num_q) + CSA_MAX_CTAS) * slot_bytes_for(k);
+         (static_cast<size_t>(args->num_q) + CSA_MAX_CTAS) * slot_bytes_fused(args->num_q, k);
 }
 
 csa_status csa_index_score(const csa_index_args* args, float* scores, int64_t score_stride, void* stream) {
@@ -1844,7 +1858,7 @@ csa_status csa_index_score_topk_fused_marked(const csa_index_args* args, int32_t
   Params P = params_of(args);
   P.ws = static_cast<uint8_t*>(ws);
   P.k = k;
-  P.slot_bytes = static_cast<int64_t>(slot_bytes_for(k));
+  P.slot_bytes = static_cast<int64_t>(slot_bytes_fused(args->num_q, k));
   P.slots_offset = static_cast<int64_t>(slots_offset_for(args->num_q));
   P.grid = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

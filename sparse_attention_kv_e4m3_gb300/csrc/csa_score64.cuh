@@ -87,6 +87,7 @@ __host__ __device__ constexpr uint32_t d_col(int s) { return 128u + 128u * stati
 static_assert(kGroupBytes % 16 == 0 && kPageBytes % 16 == 0, "group offsets and pages are 16-byte aligned");
 static_assert(kH == 64, "one N = 64 B operand per query term");
 static_assert(kCapW >= CSA_MAX_K + kTileRecs, "a cut leaves room for one more tile of keys");
+static_assert(kCapW <= kSlotKeysMax, "a workspace slot for short rows has room for the whole buffer");
 static_assert(a_col(2) <= d_col(0) && d_col(kDStages) <= kTmemCols, "TMEM column map");
 static_assert(32 % kTP == 0 && kTP == 8, "a walker ring slot holds four tiles; the issuer uses 8 lanes");
 static_assert(kThreads == 64 * (kD / 16), "the prologue splits the first query with one thread per 16 elements");
@@ -750,7 +751,11 @@ __device__ void prep_query_part(const Params& P, Smem& S, int32_t b, int qs, int
 // (16 regions, one per class and worker warp) enter a shared buffer, which is
 // cut back to between k and loose_keep(k) keys when it could overflow; each
 // segment's survivors go to workspace slot (row + CTA).
-template <int kFmt>
+// kShort: the instantiation for batches of many short rows (chunked prefill),
+// where a whole row inside the CTA that fits the buffer is written uncut when
+// its slot has room and the merge, which then reads that one slot, cuts it (the
+// selector, not the workers, bounds those batches).
+template <int kFmt, bool kShort>
 __device__ void role_select(const Params& P, Smem& S) {
   const int g = threadIdx.x - kWarpSelect * 32;
   const int sw = g >> 5, lane = g & 31;
@@ -821,10 +826,15 @@ __device__ void role_select(const Params& P, Smem& S) {
     }
     named_bar_sync(kBarSelect, 128);
     if (g == 0) mbar_arrive(smem_u32(&S.kempty[slot]));
-    shrink_if_above_reg<128, kCapW / 128, 512>(S.cand, S.scratch, kCapW - kTileRecs, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+    bool whole_short = false;
+    if constexpr (kShort)
+      whole_short = cur.tiles * kTileRecs <= kCapW && cur.lt == cur.tiles - 1 && (seg > 0 || S.plan.lt0 == 0);
+    shrink_if_above_reg<128, kCapW / 128, 512>(S.cand, S.scratch, whole_short ? kCapW : kCapW - kTileRecs, P.k,
+                                               loose_keep(P.k), &S.sel, kBarSelect, g);
     const bool seg_end = (t == S.plan.ntiles - 1) || (cur.lt == cur.tiles - 1);
     if (seg_end) {
-      shrink_if_above_reg<128, kCapW / 128, 512>(S.cand, S.scratch, loose_keep(P.k), P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
+      const int limit = whole_short ? static_cast<int>((P.slot_bytes - 16) / 8) : loose_keep(P.k);  // slot room
+      shrink_if_above_reg<128, kCapW / 128, 512>(S.cand, S.scratch, limit, P.k, loose_keep(P.k), &S.sel, kBarSelect, g);
       const int n = static_cast<int>(S.sel.n);
       uint8_t* out = P.ws + P.slots_offset + (static_cast<int64_t>(cur.b) + blockIdx.x) * P.slot_bytes;
       uint64_t* ent = reinterpret_cast<uint64_t*>(out + 16);
@@ -877,7 +887,7 @@ __device__ void prep_segments_fp4(const Params& P, Smem& S) {
 
 // ------------------------------------------------------------------ kernel
 
-template <bool kTopk, int kFmt>
+template <bool kTopk, int kFmt, bool kShort = false>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = smem_of(smem_raw);
@@ -950,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
   } else if (warp < kWarpSelect) {
     role_worker<kTopk, kFmt>(P, S);
   } else if (kTopk) {
-    role_select<kFmt>(P, S);
+    role_select<kFmt, kShort>(P, S);
   } else if (warp == kWarpSelect) {
     if constexpr (kFmt == CSA_RECORD_MXFP4)
       prep_segments_fp4(P, S);

@@ -66,6 +66,12 @@ def test_workspace_bytes_is_host_arithmetic(lib):
     # a slot holds up to min(1024, k + k/2) keys of 8 bytes after a 16-byte header
     assert native.workspace_bytes(a, 512) == 512 + slots * (16 + 8 * 768)
     assert native.workspace_bytes(a, 1000) == 512 + slots * (16 + 8 * 1024)
+    # from 512 rows the fused path takes the short-row scorer: a slot holds a whole
+    # uncut row of up to 2048 keys, whatever k
+    a.num_q = 600
+    assert native.workspace_bytes(a, 512) == 2560 + (600 + native.MAX_CTAS) * (16 + 8 * 2048)
+    assert native.workspace_bytes(a, 8) == 2560 + (600 + native.MAX_CTAS) * (16 + 8 * 2048)
+    a.num_q = 64
     assert native.workspace_bytes(a, 0) == 0
     assert native.workspace_bytes(a, native.MAX_K + 1) == 0
     a.num_q = -1

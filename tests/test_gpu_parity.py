@@ -189,6 +189,29 @@ def test_more_rows_than_sms():
     check_all(w, 32)
 
 
+# Batches of 512 rows and more take the short-row scorer: a whole row inside a CTA
+# that fits its candidate buffer (up to 2048 records) is written to its slot uncut
+# and the merge cuts it. The rows here hold 1024..2047 visible records, more than
+# a cut segment keeps, and the mixed batch adds long rows split across CTAs.
+SHORT_ROWS = {
+    "prefill_like": dict(num_q=600, history=[2100], single_request=True,
+                         q_len=lambda h, n: 1024 + (np.arange(n) * 97) % 1024, seed=43),
+    "mixed_long": dict(num_q=560, history=lambda rng, n: np.where(np.arange(n) % 70 == 0, 30000, 1800),
+                       q_len=lambda h, n: np.where(np.arange(n) % 70 == 0, h, 700 + (np.arange(n) * 53) % 1100),
+                       seed=44),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHORT_ROWS))
+@pytest.mark.parametrize("k", [40, 512])
+def test_short_row_scorer(name, k):
+    w = synth.make_workload(name, **SHORT_ROWS[name])
+    assert w.num_q >= 512
+    r = run(w, k, score=False, unfused=False)
+    assert r["status"] == 0, r["status"]
+    _parity.check_topk(w, r["idx"], r["vals"], k)
+
+
 def test_invalid_geometry_is_flagged_not_fatal():
     w = synth.make_workload("bad", num_q=4, history=[900, 900, 900, 900], seed=43)
     w.page_table[0, 2] = w.num_pages + 3      # page out of range
