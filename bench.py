@@ -355,12 +355,11 @@ def run_native(args):
     def step(mark=None):
         native.csa_index_score_topk_fused(prob, k, ws, idx, vals, stream=stream, mark=mark)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    step()  # first call: library set-up outside the warm-up
     torch.cuda.synchronize(dev)
-    if int(prob.dev_status.item()) != 0:
-        raise RuntimeError(f"device status {int(prob.dev_status.item())} after warm-up")
-
+    # The clock sampler starts before the warm-up steps, so that the GPU is not left
+    # idle between the warm-up and the timed steps (an idle GPU lowers its clocks,
+    # and the first timed steps would pay for raising them again).
     bus = None
     try:
         props = torch.cuda.get_device_properties(dev)
@@ -369,6 +368,12 @@ def run_native(args):
         pass
     sampler = ClockSampler(bus)
     time.sleep(0.3)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(prob.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(prob.dev_status.item())} after warm-up")
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     e0, e1 = E(), E()
