@@ -199,6 +199,9 @@ SHORT_ROWS = {
     "mixed_long": dict(num_q=560, history=lambda rng, n: np.where(np.arange(n) % 70 == 0, 30000, 1800),
                        q_len=lambda h, n: np.where(np.arange(n) % 70 == 0, h, 700 + (np.arange(n) * 53) % 1100),
                        seed=44),
+    # resident mode: rows of up to 30 resident pages of a longer history (whole rows in a CTA,
+    # written uncut through the selector)
+    "resident_short": dict(num_q=520, history=lambda rng, n: np.full(n, 64 * 40), resident_pages=30, seed=45),
 }
 
 
