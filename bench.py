@@ -404,14 +404,16 @@ def run_native(args):
     ms_total = e0.elapsed_time(e1)
     ms_step = ms_total / args.steps
     # the scoring kernel's own duration (roofline), from a separate loop of the same
-    # steps with an event before each call and one between its two kernels
-    n_mark = min(args.steps, 200)
+    # steps with an event before each call and one between its two kernels; the
+    # median, because the first step of the loop also holds the host's launch of
+    # that call (the GPU is idle after the synchronize until the call is enqueued)
+    n_mark = max(min(args.steps, 200), 5)
     starts, mids = [E() for _ in range(n_mark)], [E() for _ in range(n_mark)]
     for i in range(n_mark):
         starts[i].record(stream)
         step(mark=mids[i])
     torch.cuda.synchronize(dev)
-    phase1_ms = statistics.mean(starts[i].elapsed_time(mids[i]) for i in range(n_mark))
+    phase1_ms = statistics.median(starts[i].elapsed_time(mids[i]) for i in range(n_mark))
     status = int(prob.dev_status.item())
 
     keys_all, ms_max = reduce_over_ranks(keys, ms_step, dist, dev)
