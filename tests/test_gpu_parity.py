@@ -215,6 +215,21 @@ def test_short_row_scorer(name, k):
     _parity.check_topk(w, r["idx"], r["vals"], k)
 
 
+def test_short_row_scorer_edges():
+    """Exactly 512 rows (the short-row scorer's threshold): empty rows, rows shorter
+    than k (padding), rows of exactly four tiles (the whole buffer), and a page out
+    of range inside a short row (flagged; its records left out, the rest ranked)."""
+    lens = np.array([0, 5, 2048, 2047, 1, 513, 1536, 700] * 64)
+    w = synth.make_workload("edges512", num_q=512, history=lambda rng, n: np.full(n, 2048),
+                            q_len=lambda h, n: lens[:n], seed=46)
+    w.page_table[10, 20] = w.num_pages + 1  # row 10: 2048 records, one page out of range
+    r = run(w, 512, score=False, unfused=False)
+    assert r["status"] & native.DEV_PAGE_OOB
+    assert np.all(r["idx"][0] == -1) and np.all(r["vals"][0] == 0.0)
+    assert np.all(r["idx"][1, 5:] == -1)
+    _parity.check_topk(w, r["idx"], r["vals"], 512)
+
+
 def test_invalid_geometry_is_flagged_not_fatal():
     w = synth.make_workload("bad", num_q=4, history=[900, 900, 900, 900], seed=43)
     w.page_table[0, 2] = w.num_pages + 3      # page out of range
