@@ -261,6 +261,30 @@ def test_deterministic():
     assert np.array_equal(a["scores"], b["scores"], equal_nan=True)
 
 
+def test_prepared_call_repeats_the_plain_call():
+    """native.PreparedFused marshals the arguments once; each call (plain or with
+    the event between the kernels) must write what the plain binding writes,
+    also after the inputs' contents change in place between calls."""
+    w = synth.make_workload("prep", num_q=5, history=[9000, 300, 0, 20000, 4100], seed=49)
+    prob = native.Problem.from_workload(w)
+    ws = native.alloc_workspace(prob, 256, "cuda")
+    idx = torch.empty((5, 256), dtype=torch.int32, device="cuda")
+    vals = torch.empty((5, 256), dtype=torch.float32, device="cuda")
+    call = native.PreparedFused(prob, 256, ws, idx, vals)
+    for step in range(3):
+        if step == 2:  # new lengths in the same buffer
+            prob.q_len.copy_(torch.tensor([4000, 200, 0, 19000, 4100], dtype=torch.int32))
+        want_i, want_v = native.csa_index_score_topk_fused(prob, 256)
+        idx.fill_(7)
+        vals.fill_(7.0)
+        call(mark=torch.cuda.Event(enable_timing=True) if step == 1 else None)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, want_i) and torch.equal(vals, want_v), step
+    assert int(prob.dev_status.item()) == 0
+    with pytest.raises(ValueError):
+        native.PreparedFused(prob, 128, ws, idx, vals)
+
+
 def test_dev_status_optional():
     w = synth.make_workload("nostat", num_q=1, history=[500], seed=47)
     prob = native.Problem.from_workload(w, dev_status=False)
