@@ -475,11 +475,15 @@ struct CursorT {
     lt = pl.lt0;
     tiles = b < P.num_q ? query_tiles<TP>(P, b) : 0;
   }
+  // the row after b that has tiles, and its tile count
+  static __device__ __forceinline__ void next_row(const Params& P, int32_t& b, int64_t& tiles) {
+    b = next_nonempty<TP>(P, b + 1);
+    tiles = b < P.num_q ? query_tiles<TP>(P, b) : 0;
+  }
   __device__ void advance(const Params& P) {
     if (++lt >= tiles) {
-      b = next_nonempty<TP>(P, b + 1);
+      next_row(P, b, tiles);
       lt = 0;
-      tiles = b < P.num_q ? query_tiles<TP>(P, b) : 0;
     }
   }
 };
@@ -492,12 +496,12 @@ __device__ __forceinline__ bool warp_ok(bool ok) { return __shfl_sync(0xFFFFFFFF
 // Page walker: fills the ring with the PageInfo of the CTA's pages, 32 at a
 // time (TP page slots per tile; 32 / TP tiles per ring slot). SM is the
 // kernel's shared-memory struct (ring, rfull, rempty, plan, abort_flag, status).
-template <int TP, class SM>
+template <int TP, class SM, class Cur = CursorT<TP>>
 __device__ void walk_pages(const Params& P, SM& S) {
   static_assert(32 % TP == 0, "a ring slot holds whole tiles");
   const int lane = threadIdx.x & 31;
   const int64_t npg = static_cast<int64_t>(TP) * S.plan.ntiles;
-  CursorT<TP> cur;
+  Cur cur;
   cur.init(P, S.plan);
   int32_t flags = 0;
 #ifdef CSA_TEST_WALKER_DELAY_NS
@@ -521,8 +525,7 @@ __device__ void walk_pages(const Params& P, SM& S) {
     int64_t ll = cur.lt + lane / TP, tb = cur.tiles;
     while (bb < P.num_q && ll >= tb) {
       ll -= tb;
-      bb = next_nonempty<TP>(P, bb + 1);
-      tb = bb < P.num_q ? query_tiles<TP>(P, bb) : 0;
+      Cur::next_row(P, bb, tb);
     }
     PageInfo e{0, -1, 0, 0};
     if (pg + lane < npg && bb < P.num_q) e = page_of<TP>(P, bb, ll, lane % TP, &flags);

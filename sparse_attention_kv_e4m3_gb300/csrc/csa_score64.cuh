@@ -135,6 +135,41 @@ __device__ __forceinline__ uint32_t filter_word(const Smem& S, int seg) {
   return static_cast<uint32_t>(f >> 32) == static_cast<uint32_t>(seg) ? static_cast<uint32_t>(f) : 0u;
 }
 
+// The row after b that has tiles, and its tile count: the cursors' step at a
+// segment end, kept out of line so that the roles' loops stay small (the
+// parameters live in the kernel's parameter space: no copy is made).
+struct RowTiles {
+  int32_t b;
+  int64_t tiles;
+};
+__device__ __noinline__ RowTiles next_row_tiles(const Params& P, int32_t b) {
+  b = next_nonempty<kTP>(P, b + 1);
+  return {b, b < P.num_q ? query_tiles<kTP>(P, b) : 0};
+}
+
+// A role's position: row b, tile lt of its `tiles` (the segment plan's order).
+struct Cursor64 {
+  int32_t b;
+  int64_t lt;
+  int64_t tiles;
+  __device__ __forceinline__ void init(const Params& P, const Plan& pl) {
+    b = pl.b0;
+    lt = pl.lt0;
+    tiles = b < P.num_q ? query_tiles<kTP>(P, b) : 0;
+  }
+  static __device__ __forceinline__ void next_row(const Params& P, int32_t& b, int64_t& tiles) {
+    const RowTiles r = next_row_tiles(P, b);
+    b = r.b;
+    tiles = r.tiles;
+  }
+  __device__ __forceinline__ void advance(const Params& P) {
+    if (++lt >= tiles) {
+      next_row(P, b, tiles);
+      lt = 0;
+    }
+  }
+};
+
 // ------------------------------------------------------------------ issuer
 
 // Lanes 0..7 copy the 8 pages of each tile in lockstep, page j of tile t into
@@ -196,7 +231,7 @@ __device__ void role_issuer(const Params& P, Smem& S) {
 template <int kFmt>
 __device__ void role_mma(const Params& P, Smem& S, const int c) {
   constexpr int kTerms = kFmt == CSA_RECORD_MXFP4 ? 1 : 2;  // an MXFP4 query is one e4m3 term
-  CursorT<kTP> cur;
+  Cursor64 cur;
   cur.init(P, S.plan);
   const uint32_t tmem = S.tmem_base;
   int seg = 0;
@@ -614,7 +649,7 @@ __device__ void role_worker(const Params& P, Smem& S) {
   uint32_t cur_sc[2] = {0, 0}, cur_pos[2] = {0, 0}, nxt_sc[2] = {0, 0}, nxt_pos[2] = {0, 0};
   bool ok = stage(0, cur_sc, cur_pos);
 
-  CursorT<kTP> cur;
+  Cursor64 cur;
   cur.init(P, S.plan);
   int seg = 0;
   for (int64_t t = 0; ok && t < nt; ++t) {
@@ -784,7 +819,7 @@ template <int kFmt, bool kShort>
 __device__ void role_select(const Params& P, Smem& S) {
   const int g = threadIdx.x - kWarpSelect * 32;
   const int sw = g >> 5, lane = g & 31;
-  CursorT<kTP> cur;
+  Cursor64 cur;
   cur.init(P, S.plan);
   int seg = 0;
   // query preparation: the next segment to prepare (1, then 2, ...), its row,
@@ -913,7 +948,7 @@ __device__ void prep_segments_fp4(const Params& P, Smem& S) {
 // ------------------------------------------------------------------ kernel
 
 template <bool kTopk, int kFmt, bool kShort = false>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) {
+__global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = smem_of(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -981,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel_w64(const Params P) 
   } else if (warp == kWarpMma2) {
     if ((tid & 31) == 0) role_mma<kFmt>(P, S, 1);
   } else if (warp == kWarpWalker) {
-    walk_pages<kTP>(P, S);
+    walk_pages<kTP, Smem, Cursor64>(P, S);
   } else if (warp < kWarpSelect) {
     role_worker<kTopk, kFmt>(P, S);
   } else if (kTopk) {
