@@ -877,6 +877,35 @@ __device__ __forceinline__ uint64_t f2fma_(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
+// The head sum of one record (TMEM address tc: its accumulator row) when a
+// record of the warp has a negative scale: relu(s x) = |s| relu(sign(s) x), with
+// g = sign(s); the caller multiplies by |s|. Out of line: it is rare.
+template <int H>
+__device__ __noinline__ float head_sum_signed(uint32_t tc, const float4* wv, float g) {
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll 1
+  for (int c = 0; c < H; c += 32) {
+    uint32_t x[32];
+    tmem_ld16(tc + c, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+    tmem_ld16(tc + c + 16, *reinterpret_cast<uint32_t(*)[16]>(&x[16]));
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 wq = wv[(c >> 2) + j];
+      float a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = g * __uint_as_float(x[4 * j + i]);
+      acc[(2 * j) & 3] = f2fma_(f2pack_(fmaxf(a[0], 0.f), fmaxf(a[1], 0.f)), f2pack_(wq.x, wq.y), acc[(2 * j) & 3]);
+      acc[(2 * j + 1) & 3] =
+          f2fma_(f2pack_(fmaxf(a[2], 0.f), fmaxf(a[3], 0.f)), f2pack_(wq.z, wq.w), acc[(2 * j + 1) & 3]);
+    }
+  }
+  float p[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f2unpack_(acc[i], p[2 * i], p[2 * i + 1]);
+  return ((p[0] + p[4]) + (p[1] + p[5])) + ((p[2] + p[6]) + (p[3] + p[7]));
+}
+
 // One warp of a worker group: TMEM lane quarter q of every tile the group owns
 // (tiles i with i % kWorkerGroups == group). It moves its records' key bytes
 // (32 rows of each of the kSub sub-tiles) from the staged pages into the TMEM
@@ -985,7 +1014,8 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
     const float4* wv = reinterpret_cast<const float4*>(S.wbuf[seg & 1]);
     const float s = __uint_as_float(scb);
     const float g = s < 0.0f ? -1.0f : 1.0f;
-    const bool all_pos = __all_sync(0xFFFFFFFFu, g > 0.0f);
+    if (!__all_sync(0xFFFFFFFFu, g > 0.0f))  // rare: out of line, away from this loop
+      return fabsf(s) * head_sum_signed<H>(tmem + d_col<H>(td) + lane_off, wv, g);
     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll 1
     for (int c = 0; c < H; c += 32) {  // heads c .. c+31
@@ -998,7 +1028,7 @@ __device__ void role_worker(const Params& P, Smem<H>& S) {
         const float4 wq = wv[(c >> 2) + j];
         float a[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = all_pos ? __uint_as_float(x[4 * j + i]) : g * __uint_as_float(x[4 * j + i]);
+        for (int i = 0; i < 4; ++i) a[i] = __uint_as_float(x[4 * j + i]);
         acc[(2 * j) & 3] = f2fma_(f2pack_(fmaxf(a[0], 0.f), fmaxf(a[1], 0.f)), f2pack_(wq.x, wq.y), acc[(2 * j) & 3]);
         acc[(2 * j + 1) & 3] =
             f2fma_(f2pack_(fmaxf(a[2], 0.f), fmaxf(a[3], 0.f)), f2pack_(wq.z, wq.w), acc[(2 * j + 1) & 3]);
