@@ -377,15 +377,22 @@ __device__ __forceinline__ int mx_block_exp(float amax) {
 // The 8 e4m3 codes of the e2m1 magnitudes times 2^k (k <= 6), as (lo, hi) words
 // for a byte-permute lookup. For k >= -5 all eight are normal and the exponent
 // fields just move by k; below, each is converted (exact down to k = -8).
+// The table for k < -5 (blocks far below the record's largest: rare), out of
+// line so that the workers' loop stays small.
+__device__ __noinline__ uint2 e4m3_table_low(int k) {
+  const float f = pow2f(k < -40 ? -40 : k);
+  return make_uint2(e4m3x2(0.0f, 0.5f * f) | (e4m3x2(1.0f * f, 1.5f * f) << 16),
+                    e4m3x2(2.0f * f, 3.0f * f) | (e4m3x2(4.0f * f, 6.0f * f) << 16));
+}
 __device__ __forceinline__ void e4m3_table(int k, uint32_t& lo, uint32_t& hi) {
   if (k >= -5) {
     const uint32_t add = static_cast<uint32_t>(k * 8);
     lo = kE2m1ToE4m3Lo + add * 0x01010100u;  // code 0 stays 0
     hi = kE2m1ToE4m3Hi + add * 0x01010101u;
   } else {
-    const float f = pow2f(k < -40 ? -40 : k);
-    lo = e4m3x2(0.0f, 0.5f * f) | (e4m3x2(1.0f * f, 1.5f * f) << 16);
-    hi = e4m3x2(2.0f * f, 3.0f * f) | (e4m3x2(4.0f * f, 6.0f * f) << 16);
+    const uint2 t = e4m3_table_low(k);
+    lo = t.x;
+    hi = t.y;
   }
 }
 
